@@ -1,0 +1,251 @@
+"""MXAttention CPU oracle -- TEST INFRASTRUCTURE ONLY.
+
+A plain float64 restatement of the MXAttention forward pass ("MXAttention:
+Data-Free Optimal Scaling and Pre-Normalization Quantization for MXFP4
+Attention", arXiv 2607.24377, Algorithms 1 and 2, Eqs. 1-18 and 44-52, with the
+causal constraint of the MatX note "leaky quantization"). Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import it;
+the product path never does. It shares no code with the CUDA kernels.
+
+The arithmetic lives in ``mxattn_oracle.c`` (compiled on first use with gcc,
+``-ffp-contract=off`` so that the binary32 Hadamard stage is evaluated exactly
+as written). This module only marshals numpy arrays.
+
+All layouts here are *logical*: codes one per byte, scales as biased E8M0
+bytes (e + 127), Q/K scales ``[rows, 4]``, V codes ``[BH, N, 128]`` token-major
+and V scales ``[BH, 128, ceil(N/32)]``.
+
+Scale rules: 0 = UOS (ceil, Q_max = 7.25), 1 = OCP floor, 2 = TFS (ceil, 6).
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+against values and identities the pages fix (see the header of each test).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxattn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+UOS, OCP, TFS = 0, 1, 2
+PNQ, DIRECT = 0, 1
+D = 128
+BLOCK = 32
+BC = 128
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library with gcc (OpenMP if available)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:6] + ["-fopenmp"] + base[6:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            lib.orc_e2m1_value.argtypes = [I]
+            lib.orc_e2m1_value.restype = ctypes.c_double
+            lib.orc_e2m1_code.argtypes = [ctypes.c_double]
+            lib.orc_e2m1_code.restype = I
+            lib.orc_scale_exponent.argtypes = [ctypes.c_double, I]
+            lib.orc_scale_exponent.restype = I
+            lib.orc_uos_qmax.argtypes = []
+            lib.orc_uos_qmax.restype = ctypes.c_double
+            lib.orc_hadamard_fp32.argtypes = [P, P]
+            lib.orc_rotate_quantize_qk.argtypes = [P, I64, I, I, P, P]
+            lib.orc_quantize_v.argtypes = [P, I64, I64, I, P, P]
+            lib.orc_online_softmax.argtypes = [P, P, I64, P, P, P, I64, I, I, I, I, I, P, P, P, P]
+            lib.orc_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I, I, I, I, I, P, I64, P, P, P, P]
+            lib.orc_forward.restype = I
+            lib.orc_sdpa.argtypes = [P, P, P, I64, I64, I, P, I64, P]
+            lib.orc_num_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def uos_qmax() -> float:
+    return float(_load().orc_uos_qmax())
+
+
+def e2m1_value(code: int) -> float:
+    return float(_load().orc_e2m1_value(int(code)))
+
+
+def e2m1_code(v) -> np.ndarray:
+    """Elementwise E2M1 code (round to nearest, ties to even, saturate at 6)."""
+    lib = _load()
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    flat_in, flat_out = v.reshape(-1), out.reshape(-1)
+    for i in range(flat_in.size):
+        flat_out[i] = lib.orc_e2m1_code(float(flat_in[i]))
+    return out
+
+
+def scale_exponent(M: float, rule: int = UOS) -> int:
+    return int(_load().orc_scale_exponent(float(M), int(rule)))
+
+
+def hadamard_fp32(x_u16: np.ndarray) -> np.ndarray:
+    """Binary32 rotation of bf16 rows ``[..., 128]`` (given as uint16 bit patterns)."""
+    lib = _load()
+    x = _c(x_u16, np.uint16).reshape(-1, D)
+    y = np.empty(x.shape, dtype=np.float32)
+    for r in range(x.shape[0]):
+        lib.orc_hadamard_fp32(_p(x[r]), _p(y[r]))
+    return y.reshape(np.shape(x_u16))
+
+
+def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True):
+    """Alg. 2 lines 3-6. ``x_u16``: bf16 bits ``[..., 128]``.
+
+    Returns (codes ``[..., 128]`` uint8, scales ``[..., 4]`` uint8)."""
+    lib = _load()
+    x = _c(x_u16, np.uint16).reshape(-1, D)
+    rows = x.shape[0]
+    codes = np.empty((rows, D), dtype=np.uint8)
+    scales = np.empty((rows, D // BLOCK), dtype=np.uint8)
+    lib.orc_rotate_quantize_qk(_p(x), rows, int(rule), int(bool(rotate)), _p(codes), _p(scales))
+    lead = np.shape(x_u16)[:-1]
+    return codes.reshape(*lead, D), scales.reshape(*lead, D // BLOCK)
+
+
+def quantize_v(v_u16: np.ndarray, rule: int = UOS):
+    """Alg. 2 line 7 on ``[BH, N, 128]`` bf16 bits.
+
+    Returns (codes ``[BH, N, 128]``, scales ``[BH, 128, ceil(N/32)]``)."""
+    lib = _load()
+    v = _c(v_u16, np.uint16)
+    BH, N, _ = v.shape
+    nblk = (N + BLOCK - 1) // BLOCK
+    codes = np.empty((BH, N, D), dtype=np.uint8)
+    scales = np.empty((BH, D, nblk), dtype=np.uint8)
+    lib.orc_quantize_v(_p(v), BH, N, int(rule), _p(codes), _p(scales))
+    return codes, scales
+
+
+def online_softmax(q_rows, row_tok, K, V, Vraw=None, *, causal=False, quant_p=True, placement=PNQ,
+                   p_rule=UOS, bc=BC, want_phat=False):
+    """Alg. 2 lines 8-20 on real-valued inputs (float64).
+
+    ``q_rows``: ``[R, 128]``; ``row_tok``: token index of each row; ``K, V``:
+    ``[N, 128]``. Returns dict with ``out``, ``ell`` and optionally ``phat``
+    ``[R, ntiles*bc]`` and ``mhist`` ``[R, ntiles]``."""
+    lib = _load()
+    q = _c(q_rows, np.float64).reshape(-1, D)
+    tok = _c(row_tok, np.int64).reshape(-1)
+    K = _c(K, np.float64)
+    V = _c(V, np.float64)
+    Vr = None if Vraw is None else _c(Vraw, np.float64)
+    N = K.shape[0]
+    R = q.shape[0]
+    ntiles = (N + bc - 1) // bc
+    out = np.empty((R, D))
+    ell = np.empty(R)
+    phat = np.zeros((R, ntiles * bc)) if want_phat else None
+    mhist = np.full((R, ntiles), np.nan) if want_phat else None
+    lib.orc_online_softmax(_p(q), _p(tok), R, _p(K), _p(V), _p(Vr), N, int(causal), int(quant_p),
+                           int(placement), int(p_rule), int(bc), _p(out), _p(ell), _p(phat), _p(mhist))
+    res = {"out": out, "ell": ell}
+    if want_phat:
+        res["phat"] = phat
+        res["mhist"] = mhist
+    return res
+
+
+def forward(qc, qs, kc, ks, vc, vs, rows, *, vraw_u16=None, causal=False, placement=PNQ, p_rule=UOS,
+            quant_p=True, bc=BC, want_phat=False):
+    """Alg. 2 on quantized tensors in the oracle's logical layouts.
+
+    ``rows``: ``[R, 2]`` int array of (bh, token). Returns dict as
+    :func:`online_softmax`."""
+    lib = _load()
+    qc = _c(qc, np.uint8)
+    qs = _c(qs, np.uint8)
+    kc = _c(kc, np.uint8)
+    ks = _c(ks, np.uint8)
+    vc = _c(vc, np.uint8)
+    vs = _c(vs, np.uint8)
+    BH, N, _ = qc.shape
+    vr = None if vraw_u16 is None else _c(vraw_u16, np.uint16)
+    if causal and vr is None:
+        raise ValueError("causal forward needs the unquantized V (vraw_u16)")
+    rows = _c(rows, np.int64).reshape(-1, 2)
+    R = rows.shape[0]
+    ntiles = (N + bc - 1) // bc
+    out = np.empty((R, D))
+    ell = np.empty(R)
+    phat = np.zeros((R, ntiles * bc)) if want_phat else None
+    mhist = np.full((R, ntiles), np.nan) if want_phat else None
+    rc = lib.orc_forward(_p(qc), _p(qs), _p(kc), _p(ks), _p(vc), _p(vs), _p(vr), BH, N, int(causal),
+                         int(placement), int(p_rule), int(quant_p), int(bc), _p(rows), R, _p(out), _p(ell),
+                         _p(phat), _p(mhist))
+    if rc != 0:
+        raise RuntimeError(f"orc_forward failed with code {rc}")
+    res = {"out": out, "ell": ell}
+    if want_phat:
+        res["phat"] = phat
+        res["mhist"] = mhist
+    return res
+
+
+def sdpa(q_u16, k_u16, v_u16, rows, *, causal=False):
+    """Unquantized float64 attention, Eq. 1, on bf16 ``[BH, N, 128]`` inputs."""
+    lib = _load()
+    q = _c(q_u16, np.uint16)
+    k = _c(k_u16, np.uint16)
+    v = _c(v_u16, np.uint16)
+    BH, N, _ = q.shape
+    rows = _c(rows, np.int64).reshape(-1, 2)
+    out = np.empty((rows.shape[0], D))
+    lib.orc_sdpa(_p(q), _p(k), _p(v), BH, N, int(causal), _p(rows), rows.shape[0], _p(out))
+    return out
+
+
+def dequant_qk(codes, scales):
+    """Logical Q/K codes+scales -> float64 values ``[..., 128]``."""
+    vals = np.array([e2m1_value(c) for c in range(16)])
+    x = vals[np.asarray(codes)]
+    s = np.repeat(np.asarray(scales, dtype=np.int64), BLOCK, axis=-1)
+    return np.ldexp(x, s - 127)
+
+
+def dequant_v(codes, scales):
+    """Logical V codes ``[BH, N, 128]`` + scales ``[BH, 128, nblk]`` -> float64 ``[BH, N, 128]``."""
+    vals = np.array([e2m1_value(c) for c in range(16)])
+    x = vals[np.asarray(codes)]
+    N = x.shape[1]
+    s = np.repeat(np.asarray(scales, dtype=np.int64), BLOCK, axis=-1)[:, :, :N]  # [BH,128,N]
+    return np.ldexp(x, np.transpose(s, (0, 2, 1)) - 127)

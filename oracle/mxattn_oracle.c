@@ -1,0 +1,389 @@
+/*
+ * MXAttention CPU oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, float64 restatement of what the MXAttention forward pass
+ * computes, written from "MXAttention: Data-Free Optimal Scaling and
+ * Pre-Normalization Quantization for MXFP4 Attention" (arXiv 2607.24377) and
+ * the MatX note "leaky quantization" (causal section). Only the test-suite,
+ * the smoke check and the benchmark's CPU-baseline leg may load this file; the
+ * product path never does. It shares no code, header, table or constant with
+ * the CUDA kernels.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *   R1  E2M1 projection: round to nearest, ties to the even code (the code
+ *       whose mantissa bit is 0), saturating at +-6. The sign of the input is
+ *       kept, so a negative value that rounds to zero yields code 0x8.
+ *   R2  Hadamard rotation: Sylvester H_128 in natural order, R_H = H/sqrt(128),
+ *       evaluated in binary32 as seven butterfly stages h = 1,2,...,64 where
+ *       each pair (i, i+h), i&h == 0, becomes (a+b, a-b), followed by one
+ *       multiply with the binary32 value nearest 2^-3.5.
+ *   R3  UOS exponent e = ceil(log2(M/7.25)) is evaluated exactly through
+ *       frexp, then clamped to the E8M0 range [-127, 127]; it is stored as the
+ *       biased byte e+127. An all-zero block gets sigma = 1 (byte 127).
+ *   R4  Blocks: Q/K per token over channels [32b, 32b+32); V per channel over
+ *       tokens [32t, 32t+32) (last block short); P~ per query row over keys
+ *       [32t, 32t+32) counted from key 0.
+ *   R5  Online softmax with fixed key tiles of Bc = 128 in increasing key order.
+ *   R6  Causal: keys j > i are masked before the row maximum; for the 32-token
+ *       V block that holds the query itself, P^ multiplies the unquantized
+ *       (bf16) V rows instead of V^, so no later token can reach row i.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared [-fopenmp] -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_D 128
+#define ORC_BLOCK 32
+
+/* ------------------------------------------------------------------ E2M1
+ * Nonnegative E2M1 grid, Eq. (9)/(20); code index = magnitude bits.        */
+static const double kGrid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1_value(int code) {
+  double m = kGrid[code & 7];
+  return (code & 8) ? -m : m;
+}
+
+/* Round-to-nearest projection onto the finite E2M1 grid with saturation at
+ * +-6 (Eq. 10), ties to the even code (reading R1). Returns the 4-bit code. */
+int orc_e2m1_code(double v) {
+  int neg = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  if (a >= 6.0) return 7 | (neg << 3); /* out of range: saturate at +-6 (Eq. 10) */
+  int best = 0;
+  double bestd = fabs(a - kGrid[0]);
+  for (int c = 1; c < 8; c++) {
+    double d = fabs(a - kGrid[c]);
+    if (d < bestd || (d == bestd && (c % 2) == 0 && (best % 2) != 0)) {
+      best = c;
+      bestd = d;
+    }
+  }
+  return best | (neg << 3);
+}
+
+/* --------------------------------------------------------- scale rules
+ * rule 0: UOS, e = ceil(log2(M / 7.25))           (Eq. 13 / 19, Alg. 1)
+ * rule 1: OCP, e = floor(log2 M) - 2              (Eq. 11 / 97)
+ * rule 2: TFS, e = ceil(log2(M / 6))              (Eq. 14)
+ * M > 0. With M = f * 2^E, f in [0.5, 1):
+ *   ceil(log2(M/q)) = E - 3 if f <= q/8 else E - 2, for q in (4, 8];
+ *   floor(log2 M)   = E - 1.
+ * Result clamped to the E8M0 exponent range [-127, 127].                   */
+double orc_uos_qmax(void) { return 7.25; }
+
+int orc_scale_exponent(double M, int rule) {
+  int E;
+  double f = frexp(M, &E);
+  int e;
+  if (rule == 1) {
+    e = (E - 1) - 2;
+  } else {
+    double q = (rule == 2) ? 6.0 : orc_uos_qmax();
+    e = (f <= q / 8.0) ? E - 3 : E - 2;
+  }
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+/* Quantize one block of n values (Algorithm 1). codes[i] receives the 4-bit
+ * code, the return value is the biased E8M0 byte.                          */
+static int quantize_block(const double* v, int n, int rule, uint8_t* codes) {
+  double M = 0.0;
+  for (int i = 0; i < n; i++) {
+    double a = fabs(v[i]);
+    if (a > M) M = a;
+  }
+  if (M == 0.0) { /* all-zero block: sigma = 1, every element 0 */
+    for (int i = 0; i < n; i++) codes[i] = 0;
+    return 127;
+  }
+  int e = orc_scale_exponent(M, rule);
+  for (int i = 0; i < n; i++) codes[i] = (uint8_t)orc_e2m1_code(ldexp(v[i], -e));
+  return e + 127;
+}
+
+/* Dequantized value of one block element: code value times 2^(byte-127). */
+static double dq(uint8_t code, uint8_t sbyte) { return ldexp(orc_e2m1_value(code), (int)sbyte - 127); }
+
+/* --------------------------------------------------------------- bf16 */
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ------------------------------------------------------ Hadamard (R2)
+ * y = x R_H with R_H = H_128 / sqrt(128), Sylvester order. Binary32.       */
+void orc_hadamard_fp32(const uint16_t* x_bf16, float* y) {
+  float z[ORC_D];
+  for (int i = 0; i < ORC_D; i++) z[i] = bf16_to_f32(x_bf16[i]);
+  for (int h = 1; h < ORC_D; h <<= 1) {
+    for (int i = 0; i < ORC_D; i++) {
+      if (i & h) continue;
+      float a = z[i], b = z[i + h];
+      float s = a + b;
+      float d = a - b;
+      z[i] = s;
+      z[i + h] = d;
+    }
+  }
+  const float inv_sqrt_d = (float)0.08838834764831845; /* nearest binary32 to 2^-3.5 */
+  for (int i = 0; i < ORC_D; i++) y[i] = z[i] * inv_sqrt_d;
+}
+
+/* ------------------------------------------------- Q / K quantization
+ * Alg. 2 lines 3-6: rotate each token, then quantize each 32-channel block.
+ * codes: rows x 128 (one code per byte); scales: rows x 4 biased bytes.    */
+void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotate, uint8_t* codes,
+                            uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; r++) {
+    float y[ORC_D];
+    if (rotate) {
+      orc_hadamard_fp32(x + r * ORC_D, y);
+    } else {
+      for (int i = 0; i < ORC_D; i++) y[i] = bf16_to_f32(x[r * ORC_D + i]);
+    }
+    for (int b = 0; b < ORC_D / ORC_BLOCK; b++) {
+      double v[ORC_BLOCK];
+      for (int i = 0; i < ORC_BLOCK; i++) v[i] = (double)y[b * ORC_BLOCK + i];
+      scales[r * 4 + b] = (uint8_t)quantize_block(v, ORC_BLOCK, rule, codes + r * ORC_D + b * ORC_BLOCK);
+    }
+  }
+}
+
+/* ---------------------------------------------------- V quantization
+ * Alg. 2 line 7 with token blocks (R4). v: [BH][N][128] bf16.
+ * codes: [BH][N][128] (token-major, one code per byte);
+ * scales: [BH][128][nblk], nblk = ceil(N/32).                              */
+void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, uint8_t* codes, uint8_t* scales) {
+  const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t bh = 0; bh < BH; bh++) {
+    for (int64_t c = 0; c < ORC_D; c++) {
+      for (int64_t t = 0; t < nblk; t++) {
+        int64_t n0 = t * ORC_BLOCK, n1 = n0 + ORC_BLOCK < N ? n0 + ORC_BLOCK : N;
+        int n = (int)(n1 - n0);
+        double vals[ORC_BLOCK];
+        uint8_t cb[ORC_BLOCK];
+        for (int i = 0; i < n; i++) vals[i] = (double)bf16_to_f32(v[((bh * N) + n0 + i) * ORC_D + c]);
+        scales[(bh * ORC_D + c) * nblk + t] = (uint8_t)quantize_block(vals, n, rule, cb);
+        for (int i = 0; i < n; i++) codes[((bh * N) + n0 + i) * ORC_D + c] = cb[i];
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------ online softmax core
+ * Alg. 2 lines 8-20 for one query row against one head's keys, float64.
+ *   q      : 128 query values (already dequantized)
+ *   K, V   : N x 128 key / value values (already dequantized)
+ *   Vraw   : N x 128 unquantized values, used on the causal diagonal block
+ *   i      : the query's token index (causal masking and the diagonal block)
+ * Options: quant_p (PNQ quantizer on), placement (0 = PNQ: l from P^,
+ * 1 = direct: l from P~, Eq. 16-17), p_rule (scale rule for P~), bc (tile).
+ * Outputs: o[128], *ell; optional phat[ntiles*bc] (P^ of each tile before any
+ * later rescale, masked slots 0) and mhist[ntiles] (running max after each
+ * tile).                                                                    */
+typedef struct {
+  int causal;
+  int quant_p;
+  int placement;
+  int p_rule;
+  int bc;
+} orc_opts;
+
+static void online_softmax_row(const double* q, const double* K, const double* V, const double* Vraw,
+                               int64_t N, int64_t i, const orc_opts* op, double* o, double* ell_out,
+                               double* phat, double* mhist) {
+  const int bc = op->bc;
+  const double inv_sqrt_d = 1.0 / sqrt((double)ORC_D);
+  int64_t ntiles = (N + bc - 1) / bc;
+  if (op->causal) ntiles = i / bc + 1;
+  double m = -INFINITY, ell = 0.0;
+  double acc[ORC_D];
+  for (int c = 0; c < ORC_D; c++) acc[c] = 0.0;
+  double* S = (double*)malloc(sizeof(double) * bc);
+  double* Pt = (double*)malloc(sizeof(double) * bc);
+  double* Ph = (double*)malloc(sizeof(double) * bc);
+  unsigned char* valid = (unsigned char*)malloc(bc);
+  for (int64_t j = 0; j < ntiles; j++) {
+    const int64_t k0 = j * bc;
+    /* line 11: S = Q^ K^T / sqrt(d) */
+    double rowmax = -INFINITY;
+    for (int kk = 0; kk < bc; kk++) {
+      int64_t key = k0 + kk;
+      valid[kk] = (key < N) && (!op->causal || key <= i);
+      if (!valid[kk]) {
+        S[kk] = -INFINITY;
+        continue;
+      }
+      double dot = 0.0;
+      for (int c = 0; c < ORC_D; c++) dot += q[c] * K[key * ORC_D + c];
+      S[kk] = dot * inv_sqrt_d;
+      if (S[kk] > rowmax) rowmax = S[kk];
+    }
+    /* lines 12-13 */
+    double m_new = m > rowmax ? m : rowmax;
+    double alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+    /* line 14: P~ = exp(S - m_new) */
+    for (int kk = 0; kk < bc; kk++) Pt[kk] = valid[kk] ? exp(S[kk] - m_new) : 0.0;
+    /* line 15: P^ = Q*(P~), 32-key blocks counted from key 0 */
+    for (int b0 = 0; b0 < bc; b0 += ORC_BLOCK) {
+      if (op->quant_p) {
+        uint8_t cb[ORC_BLOCK];
+        int sb = quantize_block(Pt + b0, ORC_BLOCK, op->p_rule, cb);
+        for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = dq(cb[t], (uint8_t)sb);
+      } else {
+        for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = Pt[b0 + t];
+      }
+    }
+    /* line 16 (PNQ, Eq. 47) or Eq. 16 (direct) */
+    double tile_sum = 0.0;
+    for (int kk = 0; kk < bc; kk++) tile_sum += (op->placement == 0) ? Ph[kk] : Pt[kk];
+    ell = alpha * ell + tile_sum;
+    /* line 17 (Eq. 48): O = diag(alpha) O + P^ V^ */
+    for (int c = 0; c < ORC_D; c++) acc[c] *= alpha;
+    for (int kk = 0; kk < bc; kk++) {
+      if (!valid[kk] || Ph[kk] == 0.0) continue;
+      int64_t key = k0 + kk;
+      const double* vrow = (op->causal && (key / ORC_BLOCK) == (i / ORC_BLOCK)) ? Vraw + key * ORC_D
+                                                                                 : V + key * ORC_D;
+      for (int c = 0; c < ORC_D; c++) acc[c] += Ph[kk] * vrow[c];
+    }
+    m = m_new; /* line 18 */
+    if (phat) memcpy(phat + j * bc, Ph, sizeof(double) * bc);
+    if (mhist) mhist[j] = m;
+  }
+  /* line 20: O = diag(l)^-1 O */
+  for (int c = 0; c < ORC_D; c++) o[c] = acc[c] / ell;
+  *ell_out = ell;
+  free(S);
+  free(Pt);
+  free(Ph);
+  free(valid);
+}
+
+/* Entry on real-valued inputs (used by the oracle's own pins).
+ * q_rows: nrows x 128 query values; row_tok: token index of each query row.
+ * K, V, Vraw: N x 128 (Vraw may be NULL when not causal).                   */
+void orc_online_softmax(const double* q_rows, const int64_t* row_tok, int64_t nrows, const double* K,
+                        const double* V, const double* Vraw, int64_t N, int causal, int quant_p,
+                        int placement, int p_rule, int bc, double* out, double* ell, double* phat,
+                        double* mhist) {
+  orc_opts op = {causal, quant_p, placement, p_rule, bc};
+  const int64_t ntiles = (N + bc - 1) / bc;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < nrows; r++) {
+    online_softmax_row(q_rows + r * ORC_D, K, V, Vraw ? Vraw : V, N, row_tok[r], &op, out + r * ORC_D,
+                       ell + r, phat ? phat + r * ntiles * bc : NULL, mhist ? mhist + r * ntiles : NULL);
+  }
+}
+
+/* ------------------------------------------------------ full forward
+ * Alg. 2 on quantized tensors. Inputs in the oracle's logical layouts:
+ *   qc, kc, vc : [BH][N][128] codes, one per byte
+ *   qs, ks     : [BH][N][4] biased scale bytes (per token, per channel block)
+ *   vs         : [BH][128][nblk] biased scale bytes (per channel, per token block)
+ *   vraw       : [BH][N][128] bf16 values of V (causal diagonal blocks), or NULL
+ * rows: nrows pairs (bh, token). Outputs as in orc_online_softmax.
+ * Rows are grouped by head by the caller for efficiency (not required).     */
+int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const uint8_t* ks, const uint8_t* vc,
+                const uint8_t* vs, const uint16_t* vraw, int64_t BH, int64_t N, int causal, int placement,
+                int p_rule, int quant_p, int bc, const int64_t* rows, int64_t nrows, double* out, double* ell,
+                double* phat, double* mhist) {
+  if (bc <= 0 || bc % ORC_BLOCK != 0) return 1;
+  const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
+  const int64_t ntiles = (N + bc - 1) / bc;
+  orc_opts op = {causal, quant_p, placement, p_rule, bc};
+  double* K = (double*)malloc(sizeof(double) * N * ORC_D);
+  double* V = (double*)malloc(sizeof(double) * N * ORC_D);
+  double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);
+  if (!K || !V || !Vr) {
+    free(K);
+    free(V);
+    free(Vr);
+    return 2;
+  }
+  for (int64_t bh = 0; bh < BH; bh++) {
+    int any = 0;
+    for (int64_t r = 0; r < nrows; r++) any |= (rows[2 * r] == bh);
+    if (!any) continue;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++) {
+      for (int c = 0; c < ORC_D; c++) {
+        const int64_t e = (bh * N + n) * ORC_D + c;
+        K[n * ORC_D + c] = dq(kc[e], ks[(bh * N + n) * 4 + c / ORC_BLOCK]);
+        V[n * ORC_D + c] = dq(vc[e], vs[(bh * ORC_D + c) * nblk + n / ORC_BLOCK]);
+        Vr[n * ORC_D + c] = vraw ? (double)bf16_to_f32(vraw[e]) : V[n * ORC_D + c];
+      }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; r++) {
+      if (rows[2 * r] != bh) continue;
+      const int64_t i = rows[2 * r + 1];
+      double q[ORC_D];
+      for (int c = 0; c < ORC_D; c++) {
+        const int64_t e = (bh * N + i) * ORC_D + c;
+        q[c] = dq(qc[e], qs[(bh * N + i) * 4 + c / ORC_BLOCK]);
+      }
+      online_softmax_row(q, K, V, Vr, N, i, &op, out + r * ORC_D, ell + r,
+                         phat ? phat + r * ntiles * bc : NULL, mhist ? mhist + r * ntiles : NULL);
+    }
+  }
+  free(K);
+  free(V);
+  free(Vr);
+  return 0;
+}
+
+/* ------------------------------------------- unquantized attention, Eq. 1
+ * fp64 softmax(Q K^T / sqrt(d)) V on the bf16 inputs (no rotation: an
+ * orthogonal rotation leaves QK^T unchanged in exact arithmetic).
+ * q, k, v: [BH][N][128] bf16. rows: nrows (bh, token) pairs.                 */
+void orc_sdpa(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t BH, int64_t N, int causal,
+              const int64_t* rows, int64_t nrows, double* out) {
+  (void)BH;
+  const double inv_sqrt_d = 1.0 / sqrt((double)ORC_D);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < nrows; r++) {
+    const int64_t bh = rows[2 * r], i = rows[2 * r + 1];
+    const int64_t nk = causal ? i + 1 : N;
+    double* s = (double*)malloc(sizeof(double) * nk);
+    double qv[ORC_D], acc[ORC_D];
+    for (int c = 0; c < ORC_D; c++) {
+      qv[c] = bf16_to_f32(q[(bh * N + i) * ORC_D + c]);
+      acc[c] = 0.0;
+    }
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < nk; j++) {
+      double dot = 0.0;
+      for (int c = 0; c < ORC_D; c++) dot += qv[c] * bf16_to_f32(k[(bh * N + j) * ORC_D + c]);
+      s[j] = dot * inv_sqrt_d;
+      if (s[j] > mx) mx = s[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < nk; j++) {
+      double p = exp(s[j] - mx);
+      sum += p;
+      for (int c = 0; c < ORC_D; c++) acc[c] += p * bf16_to_f32(v[(bh * N + j) * ORC_D + c]);
+    }
+    for (int c = 0; c < ORC_D; c++) out[r * ORC_D + c] = acc[c] / sum;
+    free(s);
+  }
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

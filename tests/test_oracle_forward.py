@@ -1,0 +1,199 @@
+"""Pins of the oracle's online-softmax forward ("MXAttention" Algorithm 2).
+
+* quantization off, the recurrence equals softmax attention, Eq. (1)-(8)
+* one key tile: O = P^ V / sum(P^) with P^ = Q*(exp(S - rowmax)), Eq. (44)-(45)
+* Lemma 2 / Eq. (99)-(105): l and O equal the beta-weighted sums of the
+  per-tile P^, recomputed here from prefix maxima without the recurrence
+* Proposition 1, Eq. (51): induced PNQ weights sum to one
+* Appendix J, Eq. (118): l >= 1
+* V == 1 gives O == 1 under PNQ; under the direct placement of Eq. (16)-(17)
+  it does not (Eq. (110), negative control)
+* causal: perturbing tokens > i leaves row i bit-identical (MatX note); without
+  the diagonal-block rule a perturbation inside the query's own V block leaks
+"""
+import numpy as np
+import pytest
+import torch
+
+D = 128
+
+
+def _softmax_attn(q, K, V, causal_tok=None):
+    S = q @ K.T / np.sqrt(D)
+    if causal_tok is not None:
+        mask = np.arange(K.shape[0])[None, :] > np.asarray(causal_tok)[:, None]
+        S = np.where(mask, -np.inf, S)
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    return (P / P.sum(axis=1, keepdims=True)) @ V
+
+
+def _quant_block(orc, x):
+    """Algorithm 1 on a 1-D block using the oracle's pinned scalar pieces."""
+    M = np.abs(x).max()
+    if M == 0:
+        return np.zeros_like(x)
+    e = orc.scale_exponent(M, orc.UOS)
+    codes = orc.e2m1_code(x / 2.0 ** e)
+    return np.array([orc.e2m1_value(int(c)) for c in codes]) * 2.0 ** e
+
+
+@pytest.mark.parametrize("bc", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_unquantized_recurrence_equals_softmax(orc, bc, causal):
+    rng = np.random.default_rng(10 + bc)
+    N = 300
+    K, V = rng.standard_normal((N, D)), rng.standard_normal((N, D))
+    tok = np.array([0, 5, 31, 32, 127, 128, 200, 299])
+    q = rng.standard_normal((len(tok), D)) * 2
+    res = orc.online_softmax(q, tok, K, V, causal=causal, quant_p=False, bc=bc)
+    ref = _softmax_attn(q, K, V, tok if causal else None)
+    assert np.max(np.abs(res["out"] - ref)) < 1e-12
+
+
+def test_one_tile_closed_form(orc):
+    rng = np.random.default_rng(11)
+    N = 100
+    K, V = rng.standard_normal((N, D)), rng.standard_normal((N, D))
+    q = rng.standard_normal((6, D)) * 3
+    res = orc.online_softmax(q, np.zeros(6, dtype=np.int64), K, V, quant_p=True)
+    S = q @ K.T / np.sqrt(D)
+    for r in range(6):
+        Pt = np.concatenate([np.exp(S[r] - S[r].max()), np.zeros(128 - N)])
+        Ph = np.concatenate([_quant_block(orc, Pt[b:b + 32]) for b in range(0, 128, 32)])[:N]
+        ref = Ph @ V / Ph.sum()
+        assert np.allclose(res["out"][r], ref, rtol=0, atol=1e-13)
+        assert abs(res["ell"][r] - Ph.sum()) < 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_lemma2_prop1_from_prefix_maxima(orc, causal):
+    rng = np.random.default_rng(12)
+    N, bc = 700, 128
+    K, V = rng.standard_normal((N, D)), rng.standard_normal((N, D))
+    # make the running max move across tiles: the row maximum sits in a late tile
+    tok = np.array([650, 699, 300, 129])
+    q = rng.standard_normal((len(tok), D)) * 2
+    K[600] = q[0] * 0.5
+    res = orc.online_softmax(q, tok, K, V, causal=causal, quant_p=True, want_phat=True)
+    S = q @ K.T / np.sqrt(D)
+    ntiles = (N + bc - 1) // bc
+    for r, i in enumerate(tok):
+        nt = i // bc + 1 if causal else ntiles
+        valid = np.arange(ntiles * bc) < N
+        if causal:
+            valid &= np.arange(ntiles * bc) <= i
+        Srow = np.full(ntiles * bc, -np.inf)
+        Srow[:N] = S[r]
+        Srow[~valid] = -np.inf
+        m_prefix = np.maximum.accumulate([Srow[j * bc:(j + 1) * bc].max() for j in range(nt)])
+        phat_ref = np.zeros(ntiles * bc)
+        for j in range(nt):
+            Pt = np.where(valid[j * bc:(j + 1) * bc], np.exp(Srow[j * bc:(j + 1) * bc] - m_prefix[j]), 0.0)
+            phat_ref[j * bc:(j + 1) * bc] = np.concatenate([_quant_block(orc, Pt[b:b + 32]) for b in range(0, bc, 32)])
+        assert np.array_equal(res["phat"][r], phat_ref)
+        assert np.allclose(res["mhist"][r, :nt], m_prefix, rtol=0, atol=1e-12)
+        beta = np.exp(m_prefix - m_prefix[-1])                           # Eq. (99)
+        eff = np.concatenate([beta[j] * phat_ref[j * bc:(j + 1) * bc] for j in range(nt)])  # Eq. (103)-(104)
+        ell = eff.sum()                                                   # Eq. (102)
+        assert abs(res["ell"][r] - ell) <= 1e-13 * ell
+        Vp = np.zeros((ntiles * bc, D))
+        Vp[:N] = V
+        assert np.allclose(res["out"][r] * res["ell"][r], eff[:nt * bc] @ Vp[:nt * bc], rtol=1e-12, atol=1e-12)
+        P_pnq = eff / res["ell"][r]                                       # Eq. (50)
+        assert abs(P_pnq.sum() - 1.0) < 1e-14                             # Eq. (51)
+        assert res["ell"][r] >= 1.0                                       # Eq. (118)
+
+
+def test_ell_at_least_one_many_rows(orc):
+    rng = np.random.default_rng(13)
+    for scale in [0.1, 1.0, 10.0, 100.0]:
+        N = 400
+        K, V = rng.standard_normal((N, D)), rng.standard_normal((N, D))
+        q = rng.standard_normal((16, D)) * scale
+        res = orc.online_softmax(q, np.zeros(16, dtype=np.int64), K, V, quant_p=True)
+        assert np.all(res["ell"] >= 1.0)
+
+
+def test_v_ones_pnq_exact_and_direct_not(orc):
+    rng = np.random.default_rng(14)
+    N = 512
+    K = rng.standard_normal((N, D))
+    V = np.ones((N, D))
+    q = rng.standard_normal((32, D)) * 0.5  # diffuse rows: many P~ entries are rounded
+    tok = np.zeros(32, dtype=np.int64)
+    pnq = orc.online_softmax(q, tok, K, V, quant_p=True, placement=orc.PNQ)
+    assert np.all(pnq["out"] == 1.0)
+    direct = orc.online_softmax(q, tok, K, V, quant_p=True, placement=orc.DIRECT)
+    rowsum = direct["out"][:, 0]
+    assert np.max(np.abs(rowsum - 1.0)) > 1e-3   # Eq. (110): row sums differ from one
+
+
+def _bits(x):
+    t = torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _pipeline(orc, q16, k16, v16, rows, vraw=None):
+    qc, qs = orc.rotate_quantize_qk(q16)
+    kc, ks = orc.rotate_quantize_qk(k16)
+    vc, vs = orc.quantize_v(v16)
+    return orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=v16 if vraw is None else vraw, causal=True)
+
+
+def test_causal_no_future_leakage(orc):
+    rng = np.random.default_rng(15)
+    N = 300
+    q = rng.standard_normal((1, N, D)) * 2
+    k = rng.standard_normal((1, N, D)) * 2
+    v = rng.standard_normal((1, N, D))
+    rows = np.array([[0, i] for i in [0, 3, 31, 33, 100, 127, 128, 170, 255, 299]])
+    base = _pipeline(orc, _bits(q), _bits(k), _bits(v), rows)["out"]
+    for r, (_, i) in enumerate(rows):
+        q2, k2, v2 = q.copy(), k.copy(), v.copy()
+        fut = slice(i + 1, N)
+        q2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
+        k2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
+        v2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
+        pert = _pipeline(orc, _bits(q2), _bits(k2), _bits(v2), rows[r:r + 1])["out"]
+        assert np.array_equal(pert[0], base[r]), f"row {i} changed"
+
+
+def test_causal_leak_without_diagonal_rule(orc):
+    """Negative control: feeding the quantized V on the diagonal block lets a
+    later token of the same 32-token V block reach row i."""
+    rng = np.random.default_rng(16)
+    N = 64
+    q = rng.standard_normal((1, N, D))
+    k = rng.standard_normal((1, N, D))
+    v = rng.standard_normal((1, N, D))
+    i = 40
+    rows = np.array([[0, i]])
+    vc, vs = orc.quantize_v(_bits(v))
+    deq = orc.dequant_v(vc, vs)
+
+    def run(vv):
+        vc2, vs2 = orc.quantize_v(_bits(vv))
+        deq2 = orc.dequant_v(vc2, vs2)
+        qc, qs = orc.rotate_quantize_qk(_bits(q))
+        kc, ks = orc.rotate_quantize_qk(_bits(k))
+        return orc.forward(qc, qs, kc, ks, vc2, vs2, rows, vraw_u16=_bits(deq2), causal=True)["out"]
+
+    v2 = v.copy()
+    v2[0, 45, :] = 1000.0  # token 45 > 40, same 32-token block [32, 64)
+    assert not np.array_equal(run(v), run(v2))
+
+
+def test_forward_on_codes_matches_real_valued_core(orc):
+    rng = np.random.default_rng(17)
+    BH, N = 2, 260
+    q16, k16, v16 = (_bits(rng.standard_normal((BH, N, D))) for _ in range(3))
+    qc, qs = orc.rotate_quantize_qk(q16)
+    kc, ks = orc.rotate_quantize_qk(k16)
+    vc, vs = orc.quantize_v(v16)
+    rows = np.array([[1, 0], [1, 259], [0, 17]])
+    res = orc.forward(qc, qs, kc, ks, vc, vs, rows)
+    Q, Kd, Vd = orc.dequant_qk(qc, qs), orc.dequant_qk(kc, ks), orc.dequant_v(vc, vs)
+    for r, (bh, i) in enumerate(rows):
+        ref = orc.online_softmax(Q[bh, i][None], [i], Kd[bh], Vd[bh], quant_p=True)
+        assert np.array_equal(res["out"][r], ref["out"][0])
