@@ -1,0 +1,341 @@
+"""Benchmark of the MXAttention MXFP4 forward hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+mxattn_rotate_quantize_qk(Q), mxattn_rotate_quantize_qk(K), mxattn_quantize_v(V),
+mxattn_forward -- four kernel launches on one stream, inputs resident in HBM.
+
+Default workload: the video-DiT shaped configuration B=1, H=40, N=32760
+(21x30x52 latent tokens), d=128, non-causal, seeded synthetic bf16 Q, K, V
+(standard normal with 4 outlier channels x20 in Q and K). The 1.0 GB of inputs
+is larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (metric: TFLOPS = 4*B*H*N*N*d per step / time).
+  --impl reference  times the float64 CPU oracle on the host cores instead,
+                    each step a bounded sample of the same workload.
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own copy of the
+workload (the path shards by independent heads; no collective touches the
+data), timing is the max over ranks, and value is the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 attention fwd TFLOPS and % of GB300 dense FP4 peak (Wan-shaped N=32760)"
+UNIT = "TFLOPS"
+FP4_OVER_BF16_NOMINAL = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rate on GB300
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, budget_rows: int, seed: int = 0):
+    """Time the oracle on a bounded sample of workload `w`: one head's K and V
+    quantized in full plus `budget_rows` query rows through the forward.
+    Returns (seconds, flops, description, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from mxfp4_precision_attention_gb300 import workloads as W
+
+    oracle.build()
+    q, k, v = W.generate(w, device="cpu", B=1, H=1, seed=w.seed + seed)
+    qb, kb, vb = (W.as_u16(t).reshape(1, w.N, 128) for t in (q, k, v))
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(w.N, size=min(budget_rows, w.N), replace=False))
+    t0 = time.perf_counter()
+    qc, qs = oracle.rotate_quantize_qk(qb[:, toks])
+    kc, ks = oracle.rotate_quantize_qk(kb)
+    vc, vs = oracle.quantize_v(vb)
+    # the forward needs Q codes at the sampled token positions
+    qc_full = np.zeros((1, w.N, 128), dtype=np.uint8)
+    qs_full = np.full((1, w.N, 4), 127, dtype=np.uint8)
+    qc_full[:, toks], qs_full[:, toks] = qc, qs
+    rows = np.stack([np.zeros_like(toks), toks], axis=1)
+    oracle.forward(qc_full, qs_full, kc, ks, vc, vs, rows, vraw_u16=vb, causal=w.causal)
+    dt = time.perf_counter() - t0
+    if w.causal:
+        flops = float(sum(4.0 * (int(t) + 1) * 128 for t in toks))
+    else:
+        flops = 4.0 * len(toks) * w.N * 128
+    desc = (f"1 head of {w.name}: rotate+quantize {len(toks)} Q rows and all {w.N} K tokens, quantize all V, "
+            f"float64 forward for {len(toks)} query rows against all keys")
+    del torch
+    return dt, flops, desc, oracle.num_threads()
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    # calibrate the sample so that one step costs ~ args.ref_step_s seconds
+    dt, fl, _, _ = cpu_oracle_sample(w, 8)
+    per_row = max(dt / 8, 1e-4)
+    rows = int(max(8, min(4096, args.ref_step_s / per_row)))
+    for i in range(args.warmup):
+        cpu_oracle_sample(w, max(4, rows // 8), seed=100 + i)
+    times, flops = [], []
+    for i in range(args.steps):
+        dt, fl, desc, thr = cpu_oracle_sample(w, rows, seed=i)
+        times.append(dt)
+        flops.append(fl)
+    total_t, total_f = sum(times), sum(flops)
+    value = total_f / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 128, "causal": w.causal,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import mxfp4_precision_attention_gb300 as mx
+    from mxfp4_precision_attention_gb300 import workloads as W
+
+    mx.load()
+    hbm, bf16, bf16_sus, peak_src = _peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16_NOMINAL
+    B, H, N = w.B, w.H, w.N
+    q, k, v = W.generate(w, device="cuda", seed=w.seed + rank)
+    qcn, qsn = mx.qk_layout_sizes(B, H, N)
+    vcn, vsn = mx.v_layout_sizes(B, H, N)
+    dev = q.device
+    qc = torch.empty(qcn, dtype=torch.uint8, device=dev)
+    qs = torch.empty(qsn, dtype=torch.uint8, device=dev)
+    kc = torch.empty(qcn, dtype=torch.uint8, device=dev)
+    ks = torch.empty(qsn, dtype=torch.uint8, device=dev)
+    vc = torch.empty(vcn, dtype=torch.uint8, device=dev)
+    vs = torch.empty(vsn, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, N, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream()
+    n_events = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_events)]
+
+    def step(i=None):
+        e = ev[i] if i is not None else None
+        if e: e[0].record(stream)
+        mx.mxattn_rotate_quantize_qk(q, qc, qs, stream=stream)
+        mx.mxattn_rotate_quantize_qk(k, kc, ks, stream=stream)
+        if e: e[1].record(stream)
+        mx.mxattn_quantize_v(v, vc, vs, stream=stream)
+        if e: e[2].record(stream)
+        mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=w.causal, out=out, stream=stream)
+        if e: e[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    mx.mxattn_check(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    mx.mxattn_check(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+        dist.barrier()
+    qk_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_events))
+    v_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_events))
+    fwd_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(n_events))
+    flops = w.flops
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
+    e = B * H * N * 128
+    qk_bytes = 2 * (e * 2 + mx.qk_layout_sizes(B, H, N)[0] + mx.qk_layout_sizes(B, H, N)[1])
+    v_bytes = e * 2 + vcn + vsn
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        outh = torch.empty((B, H, N, 128), dtype=torch.float32).pin_memory()
+        del q, k, v, qc, qs, kc, ks, vc, vs, out
+        torch.cuda.empty_cache()
+        ws = torch.empty(mx.mxattn_workspace_bytes(B, H, N), dtype=torch.uint8, device=dev)
+        mx.mxattn_attention_host(qh, kh, vh, w.causal, outh, ws, stream=stream)
+        steps_e2e = max(1, min(args.steps, 3))
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps_e2e):
+            mx.mxattn_attention_host(qh, kh, vh, w.causal, outh, ws, stream=stream)
+        dt = time.perf_counter() - t0
+        if world > 1:
+            import torch.distributed as dist
+
+            tt = torch.tensor([dt], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dt = float(tt.item())
+        e2e = {"value": world * flops * steps_e2e / dt / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * e * 2, "d2h_bytes_per_step": e * 4, "steps": steps_e2e,
+               "api": "mxattn_attention_host (pinned host buffers, copies inside the timed region)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        dt0, _, _, _ = cpu_oracle_sample(w, 4)
+        rows = int(max(8, min(2048, args.cpu_budget_s / max(dt0 / 4, 1e-4))))
+        dt, fl, desc, thr = cpu_oracle_sample(w, rows, seed=1)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, ue8m0 scales, fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": 128, "causal": w.causal,
+                       "parallelism": f"replicas x{world} (heads shard, no collective)",
+                       "l2": "inputs 1.0 GB per step > 129 MB L2; no flush"},
+            "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
+                         "frac": fwd_tflops / fp4_peak, "traffic": None,
+                         "kernel": "mxfp4_fwd_kernel",
+                         "peak_source": f"{peak_src} bf16 {bf16:.1f} TF/s x nominal fp4/bf16 ratio {FP4_OVER_BF16_NOMINAL:g}"},
+            "breakdown_ms": {"rotate_quantize_qk_x2": qk_ms, "quantize_v": v_ms, "forward": fwd_ms},
+            "quantizer_gbs": {"qk": qk_bytes / (qk_ms * 1e-3) / 1e9, "v": v_bytes / (v_ms * 1e-3) / 1e9,
+                              "hbm_peak": hbm},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="wan_32760")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=8.0)
+    args = ap.parse_args()
+    from mxfp4_precision_attention_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * mxattn.h -- C ABI of the GB300 (sm_103a) MXAttention forward.
+ *
+ * The operation is the forward pass of "MXAttention: Data-Free Optimal Scaling
+ * and Pre-Normalization Quantization for MXFP4 Attention" (arXiv 2607.24377),
+ * Algorithm 2 (section 4.3): a fixed Hadamard rotation of Q and K, MXFP4
+ * quantization of Q, K and V with the Universal Optimal Scaling boundary
+ * e = ceil(log2(M / 7.25)) (Algorithm 1, Eq. 13/19), and a tiled online
+ * softmax (Eqs. 2-8) with Pre-Normalization Quantization of each unnormalized
+ * exponential tile (Eqs. 44-48). The causal mode follows the constraint of the
+ * MatX note "leaky quantization" (no future token may reach row i).
+ *
+ * Conventions for every entry point
+ *  - Tensors are row-major contiguous [B, H, N, D]; D must be 128.
+ *  - Pointers named *_host are host memory; every other pointer is device
+ *    memory of the current CUDA device. All device buffers are allocated,
+ *    owned and freed by the caller; the library never allocates memory.
+ *  - Device pointers must be 16-byte aligned. Inputs must be finite.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Device work
+ *    is enqueued asynchronously on it; only mxattn_check and
+ *    mxattn_attention_host synchronize.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns a status and enqueues nothing. A launch failure
+ *    returns MXATTN_ERR_CUDA. mxattn_last_error() describes the most recent
+ *    failure on the calling thread. No C++ exception crosses this boundary.
+ *  - B, H or N equal to 0 is an empty problem: MXATTN_OK, nothing launched.
+ *  - B*H must not exceed 65535.
+ *
+ * Quantized layouts (all bytes):
+ *  - Q/K codes   [B*H][N][64]: E2M1 codes, channel 2j in the low nibble of
+ *                byte j. Code = sign bit (bit 3) + magnitude index into
+ *                {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *  - V codes     [B*H][128][Npad/2], Npad = 32*ceil(N/32): channel-major,
+ *                token 2j in the low nibble of byte j (the transposed layout
+ *                the P.V tensor-core product reads).
+ *  - scales      [B*H][ceil(N/128)][512]: biased E8M0 bytes (e + 127), one
+ *                512-byte atom per 128-row tile; row r of the tile and
+ *                32-element block k sit at byte (r%32)*16 + (r/32)*4 + k.
+ *                Rows are tokens for Q/K (blocks = channel blocks) and
+ *                channels for V (blocks = 32-token blocks). Slots past N hold
+ *                127. An all-zero block has scale byte 127 and zero codes.
+ */
+#ifndef MXATTN_H
+#define MXATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXATTN_API __attribute__((visibility("default")))
+#else
+#define MXATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXATTN_OK = 0,
+  MXATTN_ERR_INVALID_ARG = 1, /* null / misaligned / overlapping pointer, negative size */
+  MXATTN_ERR_UNSUPPORTED = 2, /* D != 128, B*H > 65535, N >= 2^31 */
+  MXATTN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  MXATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (reported by mxattn_check) */
+} mxattn_status;
+
+/* Byte sizes of the quantized buffers for a [B, H, N, 128] tensor. */
+MXATTN_API size_t mxattn_qk_codes_bytes(int64_t B, int64_t H, int64_t N);  /* B*H*N*64 */
+MXATTN_API size_t mxattn_qk_scales_bytes(int64_t B, int64_t H, int64_t N); /* B*H*ceil(N/128)*512 */
+MXATTN_API size_t mxattn_v_codes_bytes(int64_t B, int64_t H, int64_t N);   /* B*H*128*Npad/2 */
+MXATTN_API size_t mxattn_v_scales_bytes(int64_t B, int64_t H, int64_t N);  /* B*H*ceil(N/128)*512 */
+
+/* Algorithm 2 lines 3-6 (with Algorithm 1): rotate every token of x by the
+ * fixed Hadamard matrix R_H = H_128/sqrt(128) (Sylvester order, binary32
+ * butterflies h = 1..64 then one multiply by the binary32 nearest 2^-3.5) and
+ * quantize each 32-channel block with the UOS scale.
+ *   x      : bf16 [B, H, N, 128] (device, read only)
+ *   codes  : mxattn_qk_codes_bytes(B,H,N) bytes (device, written)
+ *   scales : mxattn_qk_scales_bytes(B,H,N) bytes (device, written)
+ * codes/scales must not overlap x or each other. Used for Q and for K. */
+MXATTN_API mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                        void* scales, void* stream);
+
+/* Algorithm 2 line 7: quantize V in blocks of 32 consecutive tokens per
+ * channel (blocks counted from token 0; the last block is zero padded) with
+ * the UOS scale; codes are written channel-major (see layouts above).
+ *   v      : bf16 [B, H, N, 128] (device, read only)
+ *   codes  : mxattn_v_codes_bytes(B,H,N) bytes; scales: mxattn_v_scales_bytes(B,H,N) bytes */
+MXATTN_API mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                void* scales, void* stream);
+
+/* Algorithm 2 lines 8-21 on quantized operands: for every query row, key
+ * tiles of Bc = 128 in increasing order; S = Q^K^T/sqrt(d) and P^V^ on
+ * tcgen05 block-scaled MXFP4 tensor cores; running max m, rescale
+ * alpha = exp(m_old - m_new); P~ = exp(S - m_new) quantized per 32-key block
+ * with the UOS scale (PNQ) and the same P^ feeding both l += sum P^ and
+ * O += P^ V^; O = O / l.
+ *   q_codes/q_scales, k_codes/k_scales : from mxattn_rotate_quantize_qk
+ *   v_codes/v_scales                   : from mxattn_quantize_v
+ *   v_bf16 : the unquantized V (bf16 [B,H,N,128]); required when causal,
+ *            may be NULL otherwise
+ *   causal : 0 = full attention; 1 = key j visible to query i iff j <= i.
+ *            For the 32-token V block that contains i, P^ multiplies the
+ *            bf16 V rows, so no token after i can influence row i.
+ *   out    : fp32 [B, H, N, 128] (device, written) */
+MXATTN_API mxattn_status mxattn_forward(const void* q_codes, const void* q_scales, const void* k_codes, const void* k_scales,
+                             const void* v_codes, const void* v_scales, const void* v_bf16, int64_t B, int64_t H,
+                             int64_t N, int64_t D, int causal, float* out, void* stream);
+
+/* Diagnostic variant of mxattn_forward that also writes every P^ tile:
+ *   phat_codes  [B*H][N][ceil(N/128)*64]: E2M1 codes of tile j at bytes
+ *               64j..64j+63 (key 2i of the tile in the low nibble of byte i);
+ *               tiles a row never visits (causal) are left untouched
+ *   phat_scales [B*H][N][ceil(N/128)*4]: biased E8M0 byte of each 32-key block
+ * The codes are the ones that enter both l and O (before the causal
+ * diagonal-block split). Same arguments and errors as mxattn_forward. */
+MXATTN_API mxattn_status mxattn_forward_dump_phat(const void* q_codes, const void* q_scales, const void* k_codes,
+                                       const void* k_scales, const void* v_codes, const void* v_scales,
+                                       const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                                       float* out, uint8_t* phat_codes, uint8_t* phat_scales, void* stream);
+
+/* BF16 comparison path (no rotation, no quantization): the same online
+ * softmax recurrence (Eqs. 2-8) with bf16 Q, K, V and P on tcgen05 kind::f16
+ * tensor cores and fp32 accumulation; l sums the bf16-rounded P.
+ *   q, k, v : bf16 [B, H, N, 128] (device); out : fp32 [B, H, N, 128] (device) */
+MXATTN_API mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
+                                  int64_t D, int causal, float* out, void* stream);
+
+/* Device workspace needed by mxattn_attention_host for [B, H, N, 128]. */
+MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/* The whole forward from host memory: copies q/k/v (bf16 [B,H,N,128], host;
+ * page-locked memory gives full copy bandwidth) into `workspace` (device,
+ * >= mxattn_workspace_bytes, 256-byte aligned), runs
+ * mxattn_rotate_quantize_qk (Q and K), mxattn_quantize_v and mxattn_forward,
+ * copies the fp32 result to out_host, and synchronizes `stream` before
+ * returning, so out_host is ready on MXATTN_OK. */
+MXATTN_API mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, const void* v_host, int64_t B, int64_t H,
+                                    int64_t N, int64_t D, int causal, float* out_host, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/* Synchronize `stream`, then read and clear the device status word that the
+ * attention kernels set when a bounded wait expires. Returns MXATTN_OK,
+ * MXATTN_ERR_TIMEOUT or MXATTN_ERR_CUDA. */
+MXATTN_API mxattn_status mxattn_check(void* stream);
+
+/* Test hook. Bit 0 makes the next attention launches skip one internal
+ * arrival so that their bounded waits expire (the kernel records
+ * MXATTN_ERR_TIMEOUT and returns). 0 restores normal operation. */
+MXATTN_API void mxattn_set_debug_flags(uint32_t flags);
+
+/* Message describing the most recent failure on this thread ("" if none). */
+MXATTN_API const char* mxattn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXATTN_H */

@@ -1,0 +1,196 @@
+"""Python binding of libmxattn, the sm_103a MXAttention forward (include/mxattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libmxattn.so``. The functions carry the names of the C entry
+points, take PyTorch CUDA tensors (PyTorch provides device memory and the
+current stream) and raise ``MxattnError`` when the library returns an error.
+There is no CPU fallback: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MxattnError", "load", "mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward",
+    "mxattn_forward_dump_phat", "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_workspace_bytes",
+    "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
+]
+
+D = 128
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "MXATTN_OK", 1: "MXATTN_ERR_INVALID_ARG", 2: "MXATTN_ERR_UNSUPPORTED", 3: "MXATTN_ERR_CUDA",
+          4: "MXATTN_ERR_TIMEOUT"}
+
+
+class MxattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libmxattn.so."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise OSError(f"libmxattn.so not found at {path}; run mxfp4_precision_attention_gb300/build.py")
+        lib = ctypes.CDLL(path)
+        P, I64, I, U32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t
+        for name in ("mxattn_qk_codes_bytes", "mxattn_qk_scales_bytes", "mxattn_v_codes_bytes",
+                     "mxattn_v_scales_bytes", "mxattn_workspace_bytes"):
+            getattr(lib, name).argtypes = [I64, I64, I64]
+            getattr(lib, name).restype = SZ
+        lib.mxattn_rotate_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P]
+        lib.mxattn_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P]
+        lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
+        lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
+        lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
+        lib.mxattn_attention_host.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, SZ, P]
+        lib.mxattn_check.argtypes = [P]
+        lib.mxattn_set_debug_flags.argtypes = [U32]
+        lib.mxattn_set_debug_flags.restype = None
+        lib.mxattn_last_error.restype = ctypes.c_char_p
+        for name in ("mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward", "mxattn_forward_dump_phat",
+                     "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_check"):
+            getattr(lib, name).restype = I
+        _lib = lib
+        return lib
+
+
+def _raise(st: int):
+    if st != 0:
+        raise MxattnError(st, (load().mxattn_last_error() or b"").decode())
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _shape(x: torch.Tensor):
+    if x.dim() != 4:
+        raise ValueError("expected a [B, H, N, D] tensor")
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("expected a contiguous bf16 CUDA tensor")
+    return x.shape
+
+
+def qk_layout_sizes(B: int, H: int, N: int) -> tuple[int, int]:
+    lib = load()
+    return int(lib.mxattn_qk_codes_bytes(B, H, N)), int(lib.mxattn_qk_scales_bytes(B, H, N))
+
+
+def v_layout_sizes(B: int, H: int, N: int) -> tuple[int, int]:
+    lib = load()
+    return int(lib.mxattn_v_codes_bytes(B, H, N)), int(lib.mxattn_v_scales_bytes(B, H, N))
+
+
+def mxattn_rotate_quantize_qk(x: torch.Tensor, codes: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                              stream=None):
+    """Hadamard rotation + UOS MXFP4 quantization of Q or K. Returns (codes, scales) uint8 tensors."""
+    B, H, N, Dx = _shape(x)
+    nc, ns = qk_layout_sizes(B, H, N)
+    codes = torch.empty(nc, dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = torch.empty(ns, dtype=torch.uint8, device=x.device) if scales is None else scales
+    _raise(load().mxattn_rotate_quantize_qk(_ptr(x), B, H, N, Dx, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def mxattn_quantize_v(v: torch.Tensor, codes: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                      stream=None):
+    """UOS MXFP4 quantization of V in 32-token blocks. Returns (codes, scales) uint8 tensors."""
+    B, H, N, Dx = _shape(v)
+    nc, ns = v_layout_sizes(B, H, N)
+    codes = torch.empty(nc, dtype=torch.uint8, device=v.device) if codes is None else codes
+    scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
+    _raise(load().mxattn_quantize_v(_ptr(v), B, H, N, Dx, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
+                   causal: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """MXFP4 attention forward with PNQ on quantized operands. Returns fp32 [B, H, N, 128]."""
+    dev = q_codes.device
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
+    _raise(load().mxattn_forward(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+                                 _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), _ptr(out), _stream(stream)))
+    return out
+
+
+def mxattn_forward_dump_phat(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
+                             causal: bool = False, stream=None):
+    """Diagnostic forward that also returns every P^ tile (codes [B*H, N, NT*64], scales [B*H, N, NT*4])."""
+    dev = q_codes.device
+    NT = (N + 127) // 128
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+    pc = torch.zeros((B * H, N, NT * 64), dtype=torch.uint8, device=dev)
+    ps = torch.zeros((B * H, N, NT * 4), dtype=torch.uint8, device=dev)
+    _raise(load().mxattn_forward_dump_phat(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales),
+                                           _ptr(v_codes), _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal),
+                                           _ptr(out), _ptr(pc), _ptr(ps), _stream(stream)))
+    return out, pc, ps
+
+
+def mxattn_forward_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """BF16 tcgen05 attention forward (comparison path). Returns fp32 [B, H, N, 128]."""
+    B, H, N, Dx = _shape(q)
+    _shape(k)
+    _shape(v)
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=q.device) if out is None else out
+    _raise(load().mxattn_forward_bf16(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
+                                      _stream(stream)))
+    return out
+
+
+def mxattn_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load().mxattn_workspace_bytes(B, H, N))
+
+
+def mxattn_attention_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor, causal: bool,
+                          out_host: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """Whole forward from host (preferably pinned) bf16 tensors into a host fp32 tensor."""
+    B, H, N, Dx = q_host.shape
+    for t in (q_host, k_host, v_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    _raise(load().mxattn_attention_host(_ptr(q_host), _ptr(k_host), _ptr(v_host), B, H, N, Dx, int(causal),
+                                        _ptr(out_host), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+    return out_host
+
+
+def mxattn_check(stream=None) -> None:
+    """Synchronize and raise MxattnError if a kernel reported an expired bounded wait."""
+    _raise(load().mxattn_check(_stream(stream)))
+
+
+def mxattn_set_debug_flags(flags: int) -> None:
+    load().mxattn_set_debug_flags(int(flags))
+
+
+def mxattn_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, stream=None):
+    """The whole hot path on device tensors: rotate+quantize Q and K, quantize V, forward."""
+    B, H, N, _ = _shape(q)
+    qc, qs = mxattn_rotate_quantize_qk(q, stream=stream)
+    kc, ks = mxattn_rotate_quantize_qk(k, stream=stream)
+    vc, vs = mxattn_quantize_v(v, stream=stream)
+    return mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal, stream=stream)

@@ -1,0 +1,349 @@
+// extern "C" boundary of libmxattn: argument validation, the device status
+// word, tensor-map encoding and the host-buffer convenience entry point.
+// The declarations and their contracts are in include/mxattn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mxattn.h"
+#include "internal.h"
+
+namespace mxattn {
+
+__device__ int g_status_word;
+
+namespace {
+
+thread_local char t_err[512] = "";
+uint32_t g_debug_flags = 0;
+
+mxattn_status fail(mxattn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof t_err, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+mxattn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MXATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range rng(const void* p, size_t n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + n};
+}
+
+// Common shape checks. Returns MXATTN_OK and sets *empty when there is no work.
+mxattn_status check_shape(int64_t B, int64_t H, int64_t N, int64_t D, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return fail(MXATTN_ERR_INVALID_ARG, "negative size (B=%lld H=%lld N=%lld)",
+                                           (long long)B, (long long)H, (long long)N);
+  if (D != kD) return fail(MXATTN_ERR_UNSUPPORTED, "head dimension D=%lld unsupported (only 128)", (long long)D);
+  *empty = (B == 0 || H == 0 || N == 0);
+  if (*empty) return MXATTN_OK;
+  if (B * H > 65535) return fail(MXATTN_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", (long long)(B * H));
+  if (N >= (int64_t(1) << 31) - kTile) return fail(MXATTN_ERR_UNSUPPORTED, "N=%lld too large", (long long)N);
+  return MXATTN_OK;
+}
+
+mxattn_status check_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(MXATTN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(MXATTN_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return MXATTN_OK;
+}
+
+size_t qk_codes(int64_t B, int64_t H, int64_t N) { return static_cast<size_t>(B * H * N * 64); }
+size_t sf_bytes(int64_t B, int64_t H, int64_t N) {
+  return static_cast<size_t>(B * H * ceil_div(N, kTile) * kSfAtomBytes);
+}
+size_t v_codes(int64_t B, int64_t H, int64_t N) {
+  return static_cast<size_t>(B * H * kD * (ceil_div(N, kBlock) * kBlock / 2));
+}
+size_t bf16_bytes(int64_t B, int64_t H, int64_t N) { return static_cast<size_t>(B * H * N * kD * 2); }
+size_t f32_bytes(int64_t B, int64_t H, int64_t N) { return static_cast<size_t>(B * H * N * kD * 4); }
+
+#define MX_TRY(expr)                          \
+  do {                                        \
+    mxattn_status _st = (expr);               \
+    if (_st != MXATTN_OK) return _st;         \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
+                           const void* vs, const void* vb, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                           float* out, uint8_t* pc, uint8_t* ps, void* stream) {
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(qc, "q_codes"));
+  MX_TRY(check_ptr(qs, "q_scales"));
+  MX_TRY(check_ptr(kc, "k_codes"));
+  MX_TRY(check_ptr(ks, "k_scales"));
+  MX_TRY(check_ptr(vc, "v_codes"));
+  MX_TRY(check_ptr(vs, "v_scales"));
+  MX_TRY(check_ptr(out, "out"));
+  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (causal) MX_TRY(check_ptr(vb, "v_bf16 (required when causal)"));
+  if ((pc == nullptr) != (ps == nullptr)) return fail(MXATTN_ERR_INVALID_ARG, "phat dump needs both buffers");
+  if (pc) {
+    MX_TRY(check_ptr(pc, "phat_codes"));
+    MX_TRY(check_ptr(ps, "phat_scales"));
+  }
+  const Range ro = rng(out, f32_bytes(B, H, N));
+  const Range ins[] = {rng(qc, qk_codes(B, H, N)), rng(qs, sf_bytes(B, H, N)), rng(kc, qk_codes(B, H, N)),
+                       rng(ks, sf_bytes(B, H, N)),  rng(vc, v_codes(B, H, N)), rng(vs, sf_bytes(B, H, N))};
+  for (const Range& r : ins)
+    if (overlap(ro, r)) return fail(MXATTN_ERR_INVALID_ARG, "out overlaps an input buffer");
+  if (causal && overlap(ro, rng(vb, bf16_bytes(B, H, N))))
+    return fail(MXATTN_ERR_INVALID_ARG, "out overlaps v_bf16");
+  Mxfp4FwdArgs a;
+  a.q_codes = qc;
+  a.q_scales = qs;
+  a.k_codes = kc;
+  a.k_scales = ks;
+  a.v_codes = vc;
+  a.v_scales = vs;
+  a.v_bf16 = vb;
+  a.BH = B * H;
+  a.N = N;
+  a.causal = causal;
+  a.out = out;
+  a.phat_codes = pc;
+  a.phat_scales = ps;
+  a.debug_flags = g_debug_flags;
+  if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
+  cudaError_t e = launch_mxfp4_forward(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mxfp4 forward launch");
+  return MXATTN_OK;
+}
+
+}  // namespace
+
+int* device_status_ptr() {
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+cudaError_t read_and_clear_device_status(int* status, cudaStream_t s) {
+  int* d = device_status_ptr();
+  if (d == nullptr) return cudaErrorInvalidDevice;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpy(status, d, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  return cudaMemset(d, 0, sizeof(int));
+}
+
+bool encode_tensor_map(void* map, int dtype_is_bf16, int rank, void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; i++) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; i++) gs[i] = strides_bytes[i];
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUresult r = enc(static_cast<CUtensorMap*>(map),
+                         dtype_is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                         static_cast<cuuint32_t>(rank), base, gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mxattn
+
+using namespace mxattn;
+
+extern "C" {
+
+size_t mxattn_qk_codes_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : qk_codes(B, H, N); }
+size_t mxattn_qk_scales_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : sf_bytes(B, H, N); }
+size_t mxattn_v_codes_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : v_codes(B, H, N); }
+size_t mxattn_v_scales_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : sf_bytes(B, H, N); }
+
+mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                        void* scales, void* stream) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(x, "x"));
+  MX_TRY(check_ptr(codes, "codes"));
+  MX_TRY(check_ptr(scales, "scales"));
+  const Range rx = rng(x, bf16_bytes(B, H, N)), rc = rng(codes, qk_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
+  if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs))
+    return fail(MXATTN_ERR_INVALID_ARG, "x, codes and scales must not overlap");
+  cudaError_t e = launch_rotate_quantize_qk(x, B * H, N, codes, scales, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_qk launch");
+  return MXATTN_OK;
+}
+
+mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                void* scales, void* stream) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(v, "v"));
+  MX_TRY(check_ptr(codes, "codes"));
+  MX_TRY(check_ptr(scales, "scales"));
+  const Range rv = rng(v, bf16_bytes(B, H, N)), rc = rng(codes, v_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
+  if (overlap(rv, rc) || overlap(rv, rs) || overlap(rc, rs))
+    return fail(MXATTN_ERR_INVALID_ARG, "v, codes and scales must not overlap");
+  cudaError_t e = launch_quantize_v(v, B * H, N, codes, scales, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize_v launch");
+  return MXATTN_OK;
+}
+
+mxattn_status mxattn_forward(const void* q_codes, const void* q_scales, const void* k_codes, const void* k_scales,
+                             const void* v_codes, const void* v_scales, const void* v_bf16, int64_t B, int64_t H,
+                             int64_t N, int64_t D, int causal, float* out, void* stream) {
+  t_err[0] = '\0';
+  return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
+                      nullptr, nullptr, stream);
+}
+
+mxattn_status mxattn_forward_dump_phat(const void* q_codes, const void* q_scales, const void* k_codes,
+                                       const void* k_scales, const void* v_codes, const void* v_scales,
+                                       const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                                       float* out, uint8_t* phat_codes, uint8_t* phat_scales, void* stream) {
+  t_err[0] = '\0';
+  if (phat_codes == nullptr || phat_scales == nullptr)
+    return fail(MXATTN_ERR_INVALID_ARG, "phat_codes and phat_scales are required");
+  return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
+                      phat_codes, phat_scales, stream);
+}
+
+mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
+                                  int64_t D, int causal, float* out, void* stream) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(q, "q"));
+  MX_TRY(check_ptr(k, "k"));
+  MX_TRY(check_ptr(v, "v"));
+  MX_TRY(check_ptr(out, "out"));
+  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const Range ro = rng(out, f32_bytes(B, H, N));
+  if (overlap(ro, rng(q, bf16_bytes(B, H, N))) || overlap(ro, rng(k, bf16_bytes(B, H, N))) ||
+      overlap(ro, rng(v, bf16_bytes(B, H, N))))
+    return fail(MXATTN_ERR_INVALID_ARG, "out overlaps an input");
+  if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
+  Bf16FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.BH = B * H;
+  a.N = N;
+  a.causal = causal;
+  a.out = out;
+  a.debug_flags = g_debug_flags;
+  cudaError_t e = launch_bf16_forward(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "bf16 forward launch");
+  return MXATTN_OK;
+}
+
+size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+  if (B < 0 || H < 0 || N < 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return 3 * up(bf16_bytes(B, H, N)) + 2 * up(qk_codes(B, H, N)) + 3 * up(sf_bytes(B, H, N)) +
+         up(v_codes(B, H, N)) + up(f32_bytes(B, H, N));
+}
+
+mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, const void* v_host, int64_t B, int64_t H,
+                                    int64_t N, int64_t D, int causal, float* out_host, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  if (!q_host || !k_host || !v_host || !out_host) return fail(MXATTN_ERR_INVALID_ARG, "host pointer is NULL");
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(MXATTN_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < mxattn_workspace_bytes(B, H, N))
+    return fail(MXATTN_ERR_INVALID_ARG, "workspace too small (%zu < %zu)", workspace_bytes,
+                mxattn_workspace_bytes(B, H, N));
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  auto take = [&](size_t n) {
+    uint8_t* p = w;
+    w += up(n);
+    return p;
+  };
+  const size_t xb = bf16_bytes(B, H, N);
+  uint8_t *q = take(xb), *k = take(xb), *v = take(xb);
+  uint8_t *qc = take(qk_codes(B, H, N)), *kc = take(qk_codes(B, H, N));
+  uint8_t *qs = take(sf_bytes(B, H, N)), *ks = take(sf_bytes(B, H, N)), *vs = take(sf_bytes(B, H, N));
+  uint8_t* vc = take(v_codes(B, H, N));
+  float* out = reinterpret_cast<float*>(take(f32_bytes(B, H, N)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(q, q_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy q");
+  if ((e = cudaMemcpyAsync(k, k_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy k");
+  if ((e = cudaMemcpyAsync(v, v_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy v");
+  MX_TRY(mxattn_rotate_quantize_qk(q, B, H, N, D, qc, qs, stream));
+  MX_TRY(mxattn_rotate_quantize_qk(k, B, H, N, D, kc, ks, stream));
+  MX_TRY(mxattn_quantize_v(v, B, H, N, D, vc, vs, stream));
+  MX_TRY(mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, D, causal, out, stream));
+  if ((e = cudaMemcpyAsync(out_host, out, f32_bytes(B, H, N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy out");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  return MXATTN_OK;
+}
+
+mxattn_status mxattn_check(void* stream) {
+  int st = 0;
+  cudaError_t e = read_and_clear_device_status(&st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mxattn_check");
+  if (st != 0) return fail(MXATTN_ERR_TIMEOUT, "a kernel's bounded wait expired (status %d)", st);
+  return MXATTN_OK;
+}
+
+void mxattn_set_debug_flags(uint32_t flags) { g_debug_flags = flags; }
+
+const char* mxattn_last_error(void) { return t_err; }
+
+}  // extern "C"

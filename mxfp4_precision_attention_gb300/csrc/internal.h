@@ -1,0 +1,59 @@
+// Host-side declarations shared by the CUDA translation units of libmxattn.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxattn {
+
+constexpr int kD = 128;        // head dimension supported by every kernel
+constexpr int kBlock = 32;     // MX block size (elements sharing one E8M0 scale)
+constexpr int kTile = 128;     // query rows / key columns per tile (Bc)
+constexpr int kSfAtomBytes = 512;  // scale bytes per 128-row tile (128 rows x 4 blocks)
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Debug switches read by the attention kernels (set through the C ABI).
+enum : uint32_t { kDebugNeverArriveS = 1u };
+
+cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales,
+                                      cudaStream_t s);
+cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, cudaStream_t s);
+
+struct Mxfp4FwdArgs {
+  const void* q_codes;
+  const void* q_scales;
+  const void* k_codes;
+  const void* k_scales;
+  const void* v_codes;
+  const void* v_scales;
+  const void* v_bf16;  // causal diagonal blocks
+  int64_t BH, N;
+  int causal;
+  float* out;
+  uint8_t* phat_codes;   // optional diagnostic dump, [BH][N][ceil(N/128)*64]
+  uint8_t* phat_scales;  // optional diagnostic dump, [BH][N][ceil(N/128)*4]
+  uint32_t debug_flags;
+};
+cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s);
+
+struct Bf16FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t BH, N;
+  int causal;
+  float* out;
+  uint32_t debug_flags;
+};
+cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s);
+
+// Device status word written by kernels whose bounded waits expired.
+cudaError_t read_and_clear_device_status(int* status, cudaStream_t s);
+int* device_status_ptr();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool encode_tensor_map(void* map, int dtype_is_bf16, int rank, void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
+
+}  // namespace mxattn

@@ -1,0 +1,97 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol that
+include/mxattn.h declares, and rejects invalid arguments on the host before
+touching the GPU (so these run on a CPU-only machine)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import mxfp4_precision_attention_gb300 as mx
+
+    return mx.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxattn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for required in ["mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward", "mxattn_forward_bf16",
+                     "mxattn_check", "mxattn_last_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from mxfp4_precision_attention_gb300 import build
+
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\b(mxattn_[a-z0-9_]+)\b", out))
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else leaks out under the mxattn_ prefix
+    assert exported == set(_declared())
+
+
+def test_size_queries(lib):
+    assert lib.mxattn_qk_codes_bytes(1, 2, 512) == 2 * 512 * 64
+    assert lib.mxattn_qk_scales_bytes(1, 2, 512) == 2 * 4 * 512
+    assert lib.mxattn_qk_scales_bytes(1, 1, 129) == 2 * 512
+    assert lib.mxattn_v_codes_bytes(1, 1, 100) == 128 * 128 // 2
+    assert lib.mxattn_v_codes_bytes(1, 40, 32760) == 40 * 128 * 32768 // 2
+    assert lib.mxattn_v_scales_bytes(4, 32, 8192) == 128 * 64 * 512
+    assert lib.mxattn_qk_codes_bytes(-1, 1, 1) == 0
+
+
+def _err(lib):
+    return lib.mxattn_last_error().decode()
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x10008)
+    # unsupported head dim
+    assert lib.mxattn_rotate_quantize_qk(fake, 1, 1, 128, 64, fake, fake, None) == 2
+    assert "128" in _err(lib)
+    # null pointers
+    assert lib.mxattn_rotate_quantize_qk(None, 1, 1, 128, 128, fake, fake, None) == 1
+    assert lib.mxattn_quantize_v(fake, 1, 1, 128, 128, None, fake, None) == 1
+    # misaligned
+    assert lib.mxattn_quantize_v(odd, 1, 1, 128, 128, fake, fake, None) == 1
+    assert "aligned" in _err(lib)
+    # negative sizes, too many heads
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 1, -1, 128, 128, 0, fake, None) == 1
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 300, 300, 128, 128, 0, fake, None) == 2
+    # overlapping outputs
+    a = ctypes.c_void_p(0x100000)
+    assert lib.mxattn_rotate_quantize_qk(a, 1, 1, 128, 128, ctypes.c_void_p(0x100000 + 4096), fake, None) == 1
+    # causal needs the bf16 V
+    big = [ctypes.c_void_p(0x1000000 * (i + 1)) for i in range(8)]
+    assert lib.mxattn_forward(*big[:6], None, 1, 1, 128, 128, 1, big[6], None) == 1
+    assert "v_bf16" in _err(lib)
+    assert lib.mxattn_forward(*big[:6], None, 1, 1, 128, 128, 2, big[6], None) == 1
+    # dump needs both buffers
+    assert lib.mxattn_forward_dump_phat(*big[:6], None, 1, 1, 128, 128, 0, big[6], big[7], None, None) == 1
+    # host entry: workspace too small / misaligned
+    assert lib.mxattn_attention_host(fake, fake, fake, 1, 1, 128, 128, 0, fake, big[0], 16, None) == 1
+    assert lib.mxattn_attention_host(fake, fake, fake, 1, 1, 128, 128, 0, fake, ctypes.c_void_p(0x1000010),
+                                     1 << 30, None) == 1
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # N = 0 or B*H = 0: OK and nothing launched (no CUDA call is made)
+    assert lib.mxattn_rotate_quantize_qk(None, 1, 1, 0, 128, None, None, None) == 0
+    assert lib.mxattn_quantize_v(None, 0, 4, 100, 128, None, None, None) == 0
+    assert lib.mxattn_forward(None, None, None, None, None, None, None, 1, 1, 0, 128, 1, None, None) == 0
+    assert lib.mxattn_forward_bf16(None, None, None, 1, 0, 10, 128, 0, None, None) == 0

@@ -1,0 +1,255 @@
+"""GPU parity of the attention forward kernels (through the C ABI) against the oracle.
+
+MXFP4 path ("MXAttention" Algorithm 2 with PNQ): the oracle quantizes the same
+bf16 inputs on its own and runs the float64 recurrence with Bc = 128. Gates:
+  * max |O_gpu - O_oracle| <= 2e-3 * RMS(O_oracle) over the compared rows;
+  * fewer than 0.1 % of P^ entries differ (compared on the dumped P^ tiles);
+  * causal: perturbing tokens > i leaves GPU row i bit-identical (MatX note);
+  * V == 1 gives O == 1 (Proposition 1 through the kernel's own l).
+BF16 path (Eqs. 1-8): within the bound set by bf16 rounding of P (see
+test_bf16_forward_vs_exact_softmax). The bounded-wait failure path is
+exercised through the test hook of the C ABI.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import _layouts as L
+from mxfp4_precision_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL_RMS = 2e-3
+MAX_FLIP_RATE = 1e-3
+
+
+@pytest.fixture(scope="module")
+def mx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mxfp4_precision_attention_gb300 as m
+
+    m.load()
+    return m
+
+
+def _gpu_mx(mx, q, k, v, causal=False, dump=False):
+    B, H, N, _ = q.shape
+    qc, qs = mx.mxattn_rotate_quantize_qk(q)
+    kc, ks = mx.mxattn_rotate_quantize_qk(k)
+    vc, vs = mx.mxattn_quantize_v(v)
+    if dump:
+        out, pc, ps = mx.mxattn_forward_dump_phat(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal)
+        mx.mxattn_check()
+        return out, pc, ps
+    out = mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal)
+    mx.mxattn_check()
+    return out
+
+
+def _oracle(orc, q, k, v, rows, causal=False, heads=None, want_phat=False):
+    """Oracle forward for rows [(bh, i)]; only the listed heads are copied and quantized."""
+    B, H, N, _ = q.shape
+    heads = sorted(set(int(r[0]) for r in rows)) if heads is None else list(heads)
+    remap = {h: i for i, h in enumerate(heads)}
+    idx = torch.tensor(heads, device=q.device)
+    qb, kb, vb = (W.as_u16(t.reshape(B * H, N, 128).index_select(0, idx)) for t in (q, k, v))
+    qc, qs = orc.rotate_quantize_qk(qb)
+    kc, ks = orc.rotate_quantize_qk(kb)
+    vc, vs = orc.quantize_v(vb)
+    rr = np.array([[remap[int(b)], int(i)] for b, i in rows], dtype=np.int64)
+    return orc.forward(qc, qs, kc, ks, vc, vs, rr, vraw_u16=vb, causal=causal, want_phat=want_phat)
+
+
+def _gate(gpu_rows, ora_rows, what):
+    err = np.abs(gpu_rows - ora_rows).max()
+    rms = math.sqrt(np.mean(ora_rows ** 2))
+    print(f"{what}: max|err| = {err:.3e}, RMS(oracle) = {rms:.3e}, ratio = {err / rms:.3e}")
+    assert err <= TOL_REL_RMS * rms, f"{what}: max|err| {err:.3e} > {TOL_REL_RMS} * RMS {rms:.3e}"
+
+
+def _flip_rate(orc, pc, ps, ora_phat, rows, N, causal):
+    vals = np.array([orc.e2m1_value(c) for c in range(16)])
+    pcn, psn = pc.cpu().numpy(), ps.cpu().numpy()
+    gp = L.phat_values(pcn[rows[:, 0], rows[:, 1]], psn[rows[:, 0], rows[:, 1]], vals)
+    keys = np.arange(gp.shape[1])[None, :]
+    valid = keys < N
+    if causal:
+        valid = valid & (keys <= rows[:, 1:2])
+    diff = (gp != ora_phat) & valid
+    return diff.sum() / valid.sum(), diff.sum()
+
+
+def _all_rows(BH, N):
+    return np.array([[b, i] for b in range(BH) for i in range(N)], dtype=np.int64)
+
+
+@pytest.mark.parametrize("case", ["tiny_outlier_512", "diffuse_1000", "causal_700"])
+def test_forward_all_rows_and_phat(mx, orc, case):
+    if case == "tiny_outlier_512":
+        q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda")
+        causal = False
+    elif case == "diffuse_1000":
+        q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=1000)
+        causal = False
+    else:
+        q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=700, seed=9)
+        causal = True
+    B, H, N, _ = q.shape
+    out, pc, ps = _gpu_mx(mx, q, k, v, causal=causal, dump=True)
+    rows = _all_rows(B * H, N)
+    ref = _oracle(orc, q, k, v, rows, causal=causal, want_phat=True)
+    g = out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)[rows[:, 0], rows[:, 1]]
+    rate, nflip = _flip_rate(orc, pc, ps, ref["phat"], rows, N, causal)
+    print(f"{case}: P^ flip rate {rate:.2e} ({nflip} entries)")
+    assert rate < MAX_FLIP_RATE
+    _gate(g, ref["out"], case)
+
+
+def test_forward_lognormal_sampled(mx, orc):
+    w = W.WORKLOADS["lognormal_4096"]
+    q, k, v = W.generate(w, device="cuda")
+    rng = np.random.default_rng(5)
+    heads = [0, 11, 23]
+    rows = np.array([[h, i] for h in heads for i in np.concatenate([rng.integers(0, w.N, 60), [0, w.N - 1]])])
+    out = _gpu_mx(mx, q, k, v).reshape(w.B * w.H, w.N, 128)
+    ref = _oracle(orc, q, k, v, rows, heads=heads)
+    g = out.cpu().numpy().astype(np.float64)[rows[:, 0], rows[:, 1]]
+    _gate(g, ref["out"], "lognormal_4096 sampled")
+
+
+@pytest.mark.parametrize("name,nrows", [("wan_32760", 48), ("hunyuan_118800", 12), ("causal_lm_8192", 64)])
+def test_forward_full_size_sampled(mx, orc, name, nrows):
+    w = W.WORKLOADS[name]
+    q, k, v = W.generate(w, device="cuda")
+    out = _gpu_mx(mx, q, k, v, causal=w.causal).reshape(w.B * w.H, w.N, 128)
+    rng = np.random.default_rng(7)
+    BH = w.B * w.H
+    heads = sorted(set([0, BH - 1, int(rng.integers(0, BH))]))
+    per = max(1, nrows // len(heads))
+    rows = []
+    for h in heads:
+        rows += [[h, int(i)] for i in rng.integers(0, w.N, per)]
+        rows += [[h, w.N - 1], [h, (w.N - 1) // 128 * 128]]  # ragged last tile
+    rows = np.array(rows, dtype=np.int64)
+    ridx = torch.tensor(rows[:, 0] * w.N + rows[:, 1], device="cuda")
+    g = out.reshape(-1, 128).index_select(0, ridx).cpu().numpy().astype(np.float64)
+    ref = _oracle(orc, q, k, v, rows, causal=w.causal, heads=heads)
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    _gate(g, ref["out"], f"{name} sampled")
+
+
+def test_causal_no_future_leakage_gpu(mx):
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=600, seed=31)
+    base = _gpu_mx(mx, q, k, v, causal=True).clone()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    for i in [0, 5, 31, 32, 63, 100, 127, 128, 200, 255, 256, 383, 450, 599]:
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
+        n = 600 - i - 1
+        if n > 0:
+            for t in (q2, k2, v2):
+                t[:, :, i + 1:] = (torch.randn((1, 2, n, 128), generator=g, device="cuda") * 30).to(torch.bfloat16)
+        out = _gpu_mx(mx, q2, k2, v2, causal=True)
+        assert torch.equal(out[:, :, i], base[:, :, i]), f"row {i} changed"
+        # the earlier rows as well
+        assert torch.equal(out[:, :, : i + 1], base[:, :, : i + 1])
+
+
+def test_v_ones_gives_ones(mx):
+    q, k, _ = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=777)
+    v = torch.ones_like(q)
+    for causal in (False, True):
+        out = _gpu_mx(mx, q, k, v, causal=causal)
+        assert torch.max(torch.abs(out - 1.0)).item() <= 1e-6
+
+
+def test_ell_consistency_direct_vs_dump(mx, orc):
+    """l_i >= 1 (Appendix J) through the kernel: rows whose max entry sits in
+    any tile keep an exact 1 in P^; the dumped P^ shows it."""
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=300)
+    _, pc, ps = _gpu_mx(mx, q, k, v, dump=True)
+    vals = np.array([orc.e2m1_value(c) for c in range(16)])
+    P = L.phat_values(pc.cpu().numpy().reshape(-1, pc.shape[-1]), ps.cpu().numpy().reshape(-1, ps.shape[-1]), vals)
+    assert np.all(np.any(P == 1.0, axis=1))
+
+
+def _bf16_host(x):
+    return (x.float().cpu().numpy()).astype(np.float64)
+
+
+@pytest.mark.parametrize("shape,causal", [((1, 2, 512), False), ((1, 3, 1000), True), ((1, 2, 4096), False)])
+def test_bf16_forward_vs_exact_softmax(mx, orc, shape, causal):
+    """BF16 path against fp64 softmax attention (Eq. 1). Each weight carries one
+    bf16 rounding of P (relative 2^-9) and the fp32 products are exact, so
+    |O - O_ref| <= 2 * 2^-9 * max|V| bounds the error."""
+    B, H, N = shape
+    q, k, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", B=B, H=H, N=N, seed=N)
+    out = mx.mxattn_forward_bf16(q, k, v, causal=causal)
+    mx.mxattn_check()
+    rng = np.random.default_rng(1)
+    rows = np.array([[b, int(i)] for b in range(B * H) for i in np.concatenate([rng.integers(0, N, 40), [0, N - 1]])])
+    ref = orc.sdpa(W.as_u16(q).reshape(B * H, N, 128), W.as_u16(k).reshape(B * H, N, 128),
+                   W.as_u16(v).reshape(B * H, N, 128), rows, causal=causal)
+    g = out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)[rows[:, 0], rows[:, 1]]
+    vmax = float(torch.max(torch.abs(v.float())).item())
+    err = np.abs(g - ref).max()
+    print(f"bf16 {shape} causal={causal}: max|err| {err:.3e}, bound {2 * 2 ** -9 * vmax:.3e}")
+    assert err <= 2 * 2 ** -9 * vmax + 1e-5
+
+
+def test_mxfp4_error_vs_unquantized_reported(mx, orc):
+    """Error of the MXFP4 path against fp64 unquantized attention: reported, not gated."""
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda")
+    out = _gpu_mx(mx, q, k, v).reshape(2, 512, 128).cpu().numpy().astype(np.float64)
+    rows = _all_rows(2, 512)
+    ref = orc.sdpa(W.as_u16(q).reshape(2, 512, 128), W.as_u16(k).reshape(2, 512, 128),
+                   W.as_u16(v).reshape(2, 512, 128), rows)
+    g = out[rows[:, 0], rows[:, 1]]
+    rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+    print(f"MXFP4 vs unquantized fp64 attention: relative L2 error {rel:.3e}")
+    assert np.isfinite(rel)
+
+
+def test_bounded_wait_timeout_reports_and_recovers(mx):
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=256)
+    good = _gpu_mx(mx, q, k, v).clone()
+    qc, qs = mx.mxattn_rotate_quantize_qk(q)
+    kc, ks = mx.mxattn_rotate_quantize_qk(k)
+    vc, vs = mx.mxattn_quantize_v(v)
+    mx.mxattn_check()
+    mx.mxattn_set_debug_flags(1)
+    try:
+        mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 2, 256)
+        with pytest.raises(mx.MxattnError) as ei:
+            mx.mxattn_check()
+        assert ei.value.status == 4
+        mx.mxattn_forward_bf16(q, k, v)
+        with pytest.raises(mx.MxattnError):
+            mx.mxattn_check()
+    finally:
+        mx.mxattn_set_debug_flags(0)
+    # the context is still usable and results are unchanged
+    again = _gpu_mx(mx, q, k, v)
+    assert torch.equal(again, good)
+
+
+def test_host_entry_point_matches_device_path(mx):
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=333)
+    dev = _gpu_mx(mx, q, k, v, causal=True)
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    outh = torch.empty(q.shape, dtype=torch.float32).pin_memory()
+    ws = torch.empty(mx.mxattn_workspace_bytes(1, 2, 333), dtype=torch.uint8, device="cuda")
+    mx.mxattn_attention_host(qh, kh, vh, True, outh, ws)
+    assert torch.equal(outh, dev.cpu())
+
+
+def test_empty_problem(mx):
+    z = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    c, s = mx.mxattn_rotate_quantize_qk(z)
+    assert c.numel() == 0 and s.numel() == 0
+    out = mx.mxattn_forward_bf16(z, z, z)
+    assert out.shape == (1, 2, 0, 128)
