@@ -296,7 +296,7 @@ def run_ours(args, w):
             "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": 128, "causal": w.causal,
                        "parallelism": f"replicas x{world} (heads shard, no collective)",
-                       "l2": "inputs 1.0 GB per step > 129 MB L2; no flush"},
+                       "l2": f"inputs {3 * e * 2 / 1e9:.2f} GB per step vs 129 MB L2; no flush"},
             "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
                          "frac": fwd_tflops / fp4_peak, "traffic": None,
                          "kernel": "mxfp4_fwd_kernel",
@@ -321,6 +321,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="wan_32760")
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling cases)")
+    ap.add_argument("--n", type=int, default=None, help="override N (smaller profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
@@ -329,6 +331,11 @@ def main():
     from mxfp4_precision_attention_gb300 import workloads as W
 
     w = W.WORKLOADS[args.workload]
+    if args.heads is not None or args.n is not None:
+        import dataclasses
+
+        w = dataclasses.replace(w, H=args.heads or w.H, N=args.n or w.N,
+                                name=f"{w.name}[H={args.heads or w.H},N={args.n or w.N}]")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
