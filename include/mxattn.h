@@ -139,6 +139,28 @@ MXATTN_API mxattn_status mxattn_attention_host(const void* q_host, const void* k
                                     int64_t N, int64_t D, int causal, float* out_host, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/* The whole forward (Q, K rotation + quantization, V quantization, attention)
+ * for callers that cannot allocate device memory -- for instance an op behind
+ * a framework plugin interface that receives only its input and output
+ * buffers, or code running under a device-memory budget owned by another
+ * allocator. The paper has no counterpart of this entry point.
+ * Same arguments as the device-buffer path: q, k, v bf16 [B, H, N, 128],
+ * out fp32 [B, H, N, 128] (device, 16-byte aligned, caller-owned).
+ * The quantized intermediates live in one fixed device array of the library
+ * (mxattn_attention_noalloc_max_scratch_bytes() = 32 MiB), held by every GPU
+ * that uses the library until the process exits; problems needing more
+ * return MXATTN_ERR_UNSUPPORTED before anything is launched (B*H*N up to about
+ * 160 000 token-heads fits). The entry point itself calls no allocator.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture. All calls
+ * share the array and it keeps the last call's contents (nothing in it needs
+ * clearing: each call rewrites every byte it reads); calls that overlap on the
+ * GPU (different streams without ordering, or several host threads) race on
+ * it and must be serialized by the caller. */
+MXATTN_API mxattn_status mxattn_attention_noalloc(const void* q, const void* k, const void* v, int64_t B, int64_t H,
+                                                  int64_t N, int64_t D, int causal, float* out, void* stream);
+MXATTN_API size_t mxattn_attention_noalloc_max_scratch_bytes(void);
+
 /* Synchronize `stream`, then read and clear the device status word that the
  * attention kernels set when a bounded wait expires. Returns MXATTN_OK,
  * MXATTN_ERR_TIMEOUT or MXATTN_ERR_CUDA. */

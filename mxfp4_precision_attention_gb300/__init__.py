@@ -20,6 +20,7 @@ __all__ = [
     "MxattnError", "load", "mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward",
     "mxattn_forward_dump_phat", "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_workspace_bytes",
     "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
+    "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes",
 ]
 
 D = 128
@@ -59,6 +60,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_attention_host.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, SZ, P]
+        lib.mxattn_attention_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
+        lib.mxattn_attention_noalloc.restype = I
+        lib.mxattn_attention_noalloc_max_scratch_bytes.argtypes = []
+        lib.mxattn_attention_noalloc_max_scratch_bytes.restype = SZ
         lib.mxattn_check.argtypes = [P]
         lib.mxattn_set_debug_flags.argtypes = [U32]
         lib.mxattn_set_debug_flags.restype = None
@@ -176,6 +181,21 @@ def mxattn_attention_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: to
                                         _ptr(out_host), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
     return out_host
+
+
+def mxattn_attention_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool, out: torch.Tensor,
+                             stream=None) -> torch.Tensor:
+    """Whole forward using the library's fixed device scratch (no allocation by the library or here)."""
+    B, H, N, Dx = _shape(q)
+    _shape(k)
+    _shape(v)
+    _raise(load().mxattn_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
+                                           _stream(stream)))
+    return out
+
+
+def mxattn_attention_noalloc_max_scratch_bytes() -> int:
+    return int(load().mxattn_attention_noalloc_max_scratch_bytes())
 
 
 def mxattn_check(stream=None) -> None:

@@ -144,6 +144,8 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
 
 }  // namespace
 
+void set_last_error(const char* msg) { snprintf(t_err, sizeof t_err, "%s", msg); }
+
 int* device_status_ptr() {
   static int* ptrs[64] = {nullptr};
   static std::mutex mu;

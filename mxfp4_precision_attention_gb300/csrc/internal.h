@@ -52,6 +52,9 @@ cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s);
 cudaError_t read_and_clear_device_status(int* status, cudaStream_t s);
 int* device_status_ptr();
 
+// Replace the calling thread's mxattn_last_error() message.
+void set_last_error(const char* msg);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 bool encode_tensor_map(void* map, int dtype_is_bf16, int rank, void* base, const uint64_t* dims,
                        const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);

@@ -1,0 +1,109 @@
+// mxattn_attention_noalloc: the whole MXAttention forward for callers that
+// cannot allocate device memory.
+//
+// Some callers have no way to allocate: a plugin interface of a host framework
+// that hands an op only its input and output tensors, a process whose device
+// memory is fully pre-partitioned by another allocator, or a latency-critical
+// loop that must not call cudaMalloc (which can synchronize the device).
+// mxattn_attention needs intermediate buffers for the quantized Q, K and V;
+// this entry point keeps them in one file-scope device array instead, so the
+// caller only passes the bf16 inputs and the fp32 output.
+//
+// The array is static device memory of the library module: every GPU on which
+// the library is used holds kScratchBytes of it until the process exits.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/mxattn.h"
+#include "internal.h"
+
+namespace mxattn {
+
+// Maximum scratch: 32 MiB (quantized Q, K, V codes and their scale atoms).
+constexpr size_t kScratchBytes = size_t(32) << 20;
+
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// symbol is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+uint8_t* scratch_on_current_device(cudaError_t* err) {
+  static uint8_t* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  return addr[dev];
+}
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t noalloc_scratch_needed(int64_t B, int64_t H, int64_t N) {
+  return 2 * up256(mxattn_qk_codes_bytes(B, H, N)) + 2 * up256(mxattn_qk_scales_bytes(B, H, N)) +
+         up256(mxattn_v_codes_bytes(B, H, N)) + up256(mxattn_v_scales_bytes(B, H, N));
+}
+
+}  // namespace mxattn
+
+using namespace mxattn;
+
+extern "C" size_t mxattn_attention_noalloc_max_scratch_bytes(void) { return kScratchBytes; }
+
+extern "C" mxattn_status mxattn_attention_noalloc(const void* q, const void* k, const void* v, int64_t B, int64_t H,
+                                                  int64_t N, int64_t D, int causal, float* out, void* stream) {
+  if (B < 0 || H < 0 || N < 0) {
+    set_last_error("mxattn_attention_noalloc: negative size");
+    return MXATTN_ERR_INVALID_ARG;
+  }
+  if (B == 0 || H == 0 || N == 0) return MXATTN_OK;
+  const size_t need = noalloc_scratch_needed(B, H, N);
+  if (need > kScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "mxattn_attention_noalloc: B*H*N = %lld needs %zu scratch bytes, more than the fixed %zu; "
+             "use mxattn_attention_host or the separate entry points with caller buffers",
+             (long long)(B * H * N), need, kScratchBytes);
+    set_last_error(msg);
+    return MXATTN_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = cudaSuccess;
+  uint8_t* s = scratch_on_current_device(&e);
+  if (s == nullptr) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "mxattn_attention_noalloc: scratch address lookup failed: %s", cudaGetErrorString(e));
+    set_last_error(msg);
+    return MXATTN_ERR_CUDA;
+  }
+  uint8_t* qc = s;
+  uint8_t* kc = qc + up256(mxattn_qk_codes_bytes(B, H, N));
+  uint8_t* qs = kc + up256(mxattn_qk_codes_bytes(B, H, N));
+  uint8_t* ks = qs + up256(mxattn_qk_scales_bytes(B, H, N));
+  uint8_t* vc = ks + up256(mxattn_qk_scales_bytes(B, H, N));
+  uint8_t* vs = vc + up256(mxattn_v_codes_bytes(B, H, N));
+  // Every byte the forward reads is rewritten by the quantizers below, so
+  // nothing in the scratch needs clearing between calls.
+  mxattn_status st = mxattn_rotate_quantize_qk(q, B, H, N, D, qc, qs, stream);
+  if (st != MXATTN_OK) return st;
+  st = mxattn_rotate_quantize_qk(k, B, H, N, D, kc, ks, stream);
+  if (st != MXATTN_OK) return st;
+  st = mxattn_quantize_v(v, B, H, N, D, vc, vs, stream);
+  if (st != MXATTN_OK) return st;
+  return mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, D, causal, out, stream);
+}
