@@ -234,15 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_uniform(kBarSFull + s, (j >> 1) & 1);
       tc_fence_after();
       if (!my_abort) {
-        uint32_t rr[32];
-        tmem_ld32(tl + kColS + s * 128 + 64 * h, rr);
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + kColS + s * 128 + 64 * h, r0);
+        tmem_ld32(tl + kColS + s * 128 + 64 * h + 32, r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(rr[i]);
-        tmem_ld32(tl + kColS + s * 128 + 64 * h + 32, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i++) v[32 + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 32; i++) {
+          v[i] = __uint_as_float(r0[i]);
+          v[32 + i] = __uint_as_float(r1[i]);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 64; i++) v[i] = 0.0f;
@@ -269,9 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmax3(m_run, pm, other);
       const float mc = m_new * C;
       uint32_t packed[32];
+      const float2 c2 = make_float2(C, C), nmc2 = make_float2(-mc, -mc);
 #pragma unroll
-      for (int i = 0; i < 32; i++)
-        packed[i] = pack_bf16x2(ex2_approx(fmaf(v[2 * i], C, -mc)), ex2_approx(fmaf(v[2 * i + 1], C, -mc)));
+      for (int i = 0; i < 32; i++) {
+        const float2 x = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), c2, nmc2);
+        packed[i] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
+      }
       const float alpha = (j == 0) ? 0.0f : ex2_approx((m_run - m_new) * C);
       if (j >= 1) {
         // PV_{j-1} done: P buffer free and O ready for rescaling
@@ -288,15 +291,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       if (j >= 1 && !my_abort && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        const int nchunks = h ? 9 : 8;
-        for (int c = 0; c < nchunks; c++) {
-          const uint32_t col = (c < 8) ? kColO + 64 * h + 8 * c : kColL;
-          uint32_t o[8];
-          tmem_ld8(tl + col, o);
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+          uint32_t o[32];
+          tmem_ld32(tl + kColO + 64 * h + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st8(tl + col, o);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            o[i] = __float_as_uint(x.x);
+            o[i + 1] = __float_as_uint(x.y);
+          }
+          tmem_st32(tl + kColO + 64 * h + 32 * c, o);
+        }
+        if (h == 1) {
+          const uint32_t l = tmem_ld1(tl + kColL);
+          tmem_wait_ld();
+          tmem_st1(tl + kColL, __float_as_uint(__uint_as_float(l) * alpha));
         }
         tmem_wait_st();
       }
@@ -310,10 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (h == 1) {
       float l = 0.0f;
       if (!my_abort && !aborted) {
-        uint32_t o[8];
-        tmem_ld8(tl + kColL, o);
+        l = __uint_as_float(tmem_ld1(tl + kColL));
         tmem_wait_ld();
-        l = __uint_as_float(o[0]);
       }
       lsum[r] = l;
     }

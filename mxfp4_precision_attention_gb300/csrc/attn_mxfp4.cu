@@ -1,31 +1,39 @@
 // MXFP4 fused attention forward with Pre-Normalization Quantization
 // ("MXAttention", Algorithm 2 lines 8-21; Eqs. 2-8 and 44-48).
 //
-// One CTA owns one 128-row query tile of one head and walks the key tiles
-// (Bc = 128) in increasing order:
+// Per query row, key tiles of Bc = 128 in increasing order:
 //   S_j   = Q^ K^_j^T                 tcgen05.mma kind::mxf4 block_scale -> TMEM
-//   m_new = max(m, rowmax S_j / sqrt(d))
-//   P~    = exp(S_j / sqrt(d) - m_new)           (registers only)
-//   P^    = Q*(P~) per 32-key block, UOS scale   (codes + scales -> smem)
+//   m_j   = max(m_{j-1}, rowmax S_j / sqrt(d))
+//   P~    = exp(S_j / sqrt(d) - m_j)             (registers only)
+//   P^    = Q*(P~) per 32-key block, UOS scale   (codes -> smem, scales -> TMEM)
 //   O     = diag(alpha) O + P^ [V^ | 1]          tcgen05.mma kind::mxf4 -> TMEM
 // V^ is extended with 16 rows of ones, so the same MMA that accumulates P^ V^
 // also accumulates l = sum P^ in column 128 of the O tile: the row sum and the
 // output use the same quantized tile by construction (Eq. 47-48).
 //
-// Warp roles (12 warps): 0 = TMA producer, 1 = MMA issuer + TMEM owner,
-// 2-3 idle, 4-11 = softmax. Softmax warp w handles TMEM lanes 32*(w%4)..+31
-// (one query row per thread) and key half h = (w-4)/4 of every tile (keys
-// 64h..64h+63), exchanging row maxima with the other half through smem.
+// A CTA owns two 128-row query tiles (A and B) of one head and streams the
+// head's K^/V^ tiles once for both. Warp roles (12 warps):
+//   0     TMA producer (Q^ tiles once; K^, V^ tiles + scale atoms, 4-stage rings)
+//   1     QK issuer: S = Q^_g K^_j^T for g = A, B alternately into one S buffer
+//   2     PV issuer: O_g += P^_g [V^_j | 1]; also owns TMEM
+//   3     idle
+//   4-7   softmax of tile A, 8-11 softmax of tile B: one full query row per
+//         thread (TMEM lanes 32*(w%4)..+31), so no cross-warp reduction is
+//         needed, and the two groups run out of phase with each other.
+// TMEM (464 of 512 columns): S 128 | O_A 144 | O_B 144 | scale factors.
+// P^ scales are written by the softmax threads straight into TMEM
+// (tcgen05.st): an M=128 block-scaled MMA reads row r's A scales from lane r,
+// column base + r/32.
 //
 // Causal mode (MatX note "leaky quantization"): keys j > i are masked before
 // the maximum, tiles past the diagonal are skipped, and for the 32-token V
-// block holding the query, P^ multiplies the bf16 V rows instead of V^ (that
-// product is formed on CUDA cores in the epilogue; the block's P^ codes are
-// zeroed in the tensor-core operand and its sum is added to l separately).
+// block holding the query, P^ multiplies the bf16 V rows instead of V^ (formed
+// on CUDA cores in the epilogue from the codes the thread kept; the block's
+// codes are zeroed in the tensor-core operand and its sum is added to l).
 //
 // Every mbarrier wait is bounded (~1 s); on expiry the kernel records an error
-// in the device status word, votes all softmax threads out of the loop, and
-// releases TMEM before returning.
+// in the device status word, the waiting warp leaves its loop, and TMEM is
+// released before the CTA returns.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -37,28 +45,22 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kKStages = 4;
 constexpr int kVStages = 4;
-constexpr int kOnesRows = 16;                   // extra B rows of ones -> l in column 128
-constexpr int kPvN = kD + kOnesRows;            // 144
+constexpr int kOnesRows = 16;                    // extra B rows of ones -> l in column 128
+constexpr int kPvN = kD + kOnesRows;             // 144
 constexpr uint32_t kTileBytes = kTile * kD / 2;  // 8192 bytes of packed E2M1
 constexpr uint32_t kVTileBytes = kPvN * kD / 2;  // 9216
 
 // shared memory carve-up (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;
-constexpr uint32_t kOffQSF = kOffP + 2 * kTileBytes;
-constexpr uint32_t kOffKSF = kOffQSF + kSfAtomBytes;
-constexpr uint32_t kOffVSF = kOffKSF + kKStages * kSfAtomBytes;
-constexpr uint32_t kOffPSF = kOffVSF + kVStages * 2 * kSfAtomBytes;
-constexpr uint32_t kOffXchg = kOffPSF + 2 * kSfAtomBytes;   // [2 buf][2 half][128] float
-constexpr uint32_t kOffLsum = kOffXchg + 2 * 2 * kTile * 4;
-constexpr uint32_t kOffLx = kOffLsum + kTile * 4;
-constexpr int kPdiagStride = 33;                             // floats per row (+1 pad)
-constexpr uint32_t kOffPdiag = kOffLx + kTile * 4;
-constexpr uint32_t kOffVdiag = kOffPdiag + kTile * kPdiagStride * 4;  // bf16 [128][128]
-constexpr uint32_t kOffBars = kOffVdiag + kTile * kD * 2;
-constexpr int kNumBars = 32;
+constexpr uint32_t kOffQ = 0;                                 // 2 tiles
+constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;            // kKStages tiles
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;     // kVStages tiles (+ ones rows)
+constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]
+constexpr uint32_t kOffQSF = kOffP + 4 * kTileBytes;          // 2 atoms
+constexpr uint32_t kOffKSF = kOffQSF + 2 * kSfAtomBytes;      // kKStages atoms
+constexpr uint32_t kOffVSF = kOffKSF + kKStages * kSfAtomBytes;  // kVStages atoms
+constexpr uint32_t kOffOnesSF = kOffVSF + kVStages * kSfAtomBytes;  // constant atom (byte 127)
+constexpr uint32_t kOffBars = kOffOnesSF + kSfAtomBytes;
+constexpr int kNumBars = 40;
 constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 
@@ -68,20 +70,20 @@ constexpr int kBarKFull = 1;
 constexpr int kBarKEmpty = kBarKFull + kKStages;
 constexpr int kBarVFull = kBarKEmpty + kKStages;
 constexpr int kBarVEmpty = kBarVFull + kVStages;
-constexpr int kBarSFull = kBarVEmpty + kVStages;
-constexpr int kBarSEmpty = kBarSFull + 2;
-constexpr int kBarPFull = kBarSEmpty + 2;
-constexpr int kBarPEmpty = kBarPFull + 2;
-constexpr int kBarODone = kBarPEmpty + 2;
-static_assert(kBarODone < kNumBars, "barrier space");
+constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2 groups]: S holds S_g of the next tile
+constexpr int kBarSEmpty = kBarSFull + 2;         // 4 arrivals: the S buffer was read
+constexpr int kBarPFull = kBarSEmpty + 1;         // [2 groups], 4 arrivals: P^ tile + O rescale ready
+constexpr int kBarPEmpty = kBarPFull + 2;         // [2 groups][2 buffers]: P^ buffer free
+constexpr int kBarODone = kBarPEmpty + 4;         // [2 groups]: P^V^ into O_g complete
+static_assert(kBarODone + 2 <= kNumBars, "barrier space");
 
 // TMEM columns
-constexpr uint32_t kColS = 0;      // 2 x 128
-constexpr uint32_t kColO = 256;    // 144
-constexpr uint32_t kColSFQ = 400;  // 4
-constexpr uint32_t kColSFK = 404;  // 2 x 4
-constexpr uint32_t kColSFP = 412;  // 2 x 4
-constexpr uint32_t kColSFV = 420;  // 2 x 8
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;                 // O_g at kColO + g * kPvN (144 each)
+constexpr uint32_t kColSFQ = 416;               // [2 groups] x 4
+constexpr uint32_t kColSFK = 424;               // [2 buffers] x 4
+constexpr uint32_t kColSFP = 432;               // [2 groups][2 buffers] x 4
+constexpr uint32_t kColSFV = 448;               // [2 buffers] x 8 (upper 4: constant ones atom)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -109,15 +111,14 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
+// max over 32 values as a shallow tree of 3-input maxima
+__device__ __forceinline__ float max32(const float* v) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; i++) a[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = fmaxf(v[30], v[31]);
+  const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]), b2 = fmax3(a[6], a[7], a[8]);
+  return fmaxf(fmax3(b0, b1, b2), fmaxf(a[9], a[10]));
 }
 
 __device__ __forceinline__ float e2m1_decode(uint32_t nib) {
@@ -146,9 +147,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int bh = blockIdx.y;
+  const int npairs = (p.NT + 1) / 2;
   // causal: heaviest query tiles first
-  const int qt = p.causal ? (p.NT - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int T = p.causal ? qt + 1 : p.NT;
+  const int pair = p.causal ? (npairs - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int qtile0 = 2 * pair, qtile1 = 2 * pair + 1;
+  const bool has_b = qtile1 < p.NT;
+  const int ntiles0 = p.causal ? qtile0 + 1 : p.NT;
+  const int ntiles1 = has_b ? (p.causal ? qtile1 + 1 : p.NT) : 0;
+  const int T = ntiles0 > ntiles1 ? ntiles0 : ntiles1;  // key tiles streamed by this CTA
   const int64_t N = p.N;
 
   // ------------------------------------------------------------ setup
@@ -163,30 +169,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
-    for (int b = 0; b < 2; b++) {
-      mbar_init(bar(kBarSFull + b), 1);
-      mbar_init(bar(kBarSEmpty + b), 8);
-      mbar_init(bar(kBarPFull + b), 8);
-      mbar_init(bar(kBarPEmpty + b), 1);
+    for (int g = 0; g < 2; g++) {
+      mbar_init(bar(kBarSFull + g), 1);
+      mbar_init(bar(kBarPFull + g), 4);
+      mbar_init(bar(kBarODone + g), 1);
+      mbar_init(bar(kBarPEmpty + 2 * g), 1);
+      mbar_init(bar(kBarPEmpty + 2 * g + 1), 1);
     }
-    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarSEmpty), 4);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 2) {
     tmem_alloc(smem_u32(tmem_base_slot), kTmemCols);
     tmem_relinquish();
   }
   if (warp >= 4) {
-    // constant parts of every V stage: 16 rows of ones (E2M1 1.0 = code 2) and
-    // their scale atom (byte 127 = 2^0); also the P^ diagonal scratch.
+    // constant operand parts: 16 rows of ones (E2M1 1.0 = code 2) under every V
+    // stage and the scale atom that goes with them (byte 127 = 2^0)
     const int t = threadIdx.x - 128;
     for (int s = 0; s < kVStages; s++) {
       uint32_t* ones = reinterpret_cast<uint32_t*>(smem + kOffV + s * kVTileBytes + kTileBytes);
       for (int i = t; i < kOnesRows * kD / 8; i += 256) ones[i] = 0x22222222u;
-      uint32_t* sf1 = reinterpret_cast<uint32_t*>(smem + kOffVSF + s * 2 * kSfAtomBytes + kSfAtomBytes);
-      for (int i = t; i < kSfAtomBytes / 4; i += 256) sf1[i] = 0x7F7F7F7Fu;
     }
-    reinterpret_cast<float*>(smem + kOffLx)[t % kTile] = 0.0f;
+    uint32_t* sf1 = reinterpret_cast<uint32_t*>(smem + kOffOnesSF);
+    for (int i = t; i < kSfAtomBytes / 4; i += 256) sf1[i] = 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -200,10 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(bar(kBarQFull), kTileBytes + kSfAtomBytes);
-      tma_load_3d(sb + kOffQ, &tm_q, bar(kBarQFull), 0, qt * kTile, bh);
-      bulk_load(sb + kOffQSF, p.q_scales + (static_cast<int64_t>(bh) * p.NT + qt) * kSfAtomBytes, kSfAtomBytes,
-                bar(kBarQFull));
+      const int ng = has_b ? 2 : 1;
+      mbar_arrive_expect_tx(bar(kBarQFull), ng * (kTileBytes + kSfAtomBytes));
+      for (int g = 0; g < ng; g++) {
+        const int qtg = g ? qtile1 : qtile0;
+        tma_load_3d(sb + kOffQ + g * kTileBytes, &tm_q, bar(kBarQFull), 0, qtg * kTile, bh);
+        bulk_load(sb + kOffQSF + g * kSfAtomBytes,
+                  p.q_scales + (static_cast<int64_t>(bh) * p.NT + qtg) * kSfAtomBytes, kSfAtomBytes,
+                  bar(kBarQFull));
+      }
       int nk = 0, nv = 0;
       for (int j = 0; j < T; j++) {
         const int ks = j % kKStages, ku = j / kKStages;
@@ -224,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(bar(kBarVFull + vs), kTileBytes + kSfAtomBytes);
         tma_load_3d(sb + kOffV + vs * kVTileBytes, &tm_v, bar(kBarVFull + vs), j * (kTile / 2), 0, bh);
-        bulk_load(sb + kOffVSF + vs * 2 * kSfAtomBytes,
+        bulk_load(sb + kOffVSF + vs * kSfAtomBytes,
                   p.v_scales + (static_cast<int64_t>(bh) * p.NT + j) * kSfAtomBytes, kSfAtomBytes,
                   bar(kBarVFull + vs));
         nv++;
@@ -236,72 +247,94 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(kBarVFull + j % kVStages), (j / kVStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer
+    // --------------------------------------------------------- QK issuer
     if (lane == 0) {
-      const uint32_t idesc_s0 = idesc_mxf4(128, kTile, 0, 0), idesc_s1 = idesc_mxf4(128, kTile, 2, 2);
-      const uint32_t idesc_o0 = idesc_mxf4(128, kPvN, 0, 0), idesc_o1 = idesc_mxf4(128, kPvN, 2, 2);
+      const uint32_t id0 = idesc_mxf4(128, kTile, 0, 0), id1 = idesc_mxf4(128, kTile, 2, 2);
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
       if (ok) {
         tc_fence_after();
         tc_cp_sf(tmem + kColSFQ, smem_desc(sb + kOffQSF, 0, 128, kSwizzleNone));
+        if (has_b) tc_cp_sf(tmem + kColSFQ + 4, smem_desc(sb + kOffQSF + kSfAtomBytes, 0, 128, kSwizzleNone));
       }
-      auto issue_pv = [&](int t) -> bool {
-        const int pb = t & 1, vs = t % kVStages;
-        if (!mbar_wait(bar(kBarPFull + pb), (t >> 1) & 1, abort_flag)) return false;
-        if (!mbar_wait(bar(kBarVFull + vs), (t / kVStages) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sfp = tmem + kColSFP + 4 * pb, sfv = tmem + kColSFV + 8 * pb;
-        tc_cp_sf(sfp, smem_desc(sb + kOffPSF + pb * kSfAtomBytes, 0, 128, kSwizzleNone));
-        tc_cp_sf(sfv, smem_desc(sb + kOffVSF + vs * 2 * kSfAtomBytes, 0, 128, kSwizzleNone));
-        tc_cp_sf(sfv + 4, smem_desc(sb + kOffVSF + vs * 2 * kSfAtomBytes + kSfAtomBytes, 0, 128, kSwizzleNone));
-        const uint32_t pa = sb + kOffP + pb * kTileBytes, va = sb + kOffV + vs * kVTileBytes;
-        mma_mxf4(tmem + kColO, smem_desc(pa, 16, 512, kSwizzle64B), smem_desc(va, 16, 512, kSwizzle64B), idesc_o0,
-                 sfp, sfv, t > 0 ? 1u : 0u);
-        mma_mxf4(tmem + kColO, smem_desc(pa + 32, 16, 512, kSwizzle64B), smem_desc(va + 32, 16, 512, kSwizzle64B),
-                 idesc_o1, sfp, sfv, 1u);
-        tc_commit(bar(kBarODone));
-        tc_commit(bar(kBarPEmpty + pb));
-        tc_commit(bar(kBarVEmpty + vs));
-        return true;
-      };
+      int n = 0;  // S productions so far
       for (int j = 0; ok && j < T; j++) {
-        const int ks = j % kKStages, s = j & 1;
+        const int ks = j % kKStages;
         if (!mbar_wait(bar(kBarKFull + ks), (j / kKStages) & 1, abort_flag)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(bar(kBarSEmpty + s), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sfk = tmem + kColSFK + 4 * s;
+        const uint32_t sfk = tmem + kColSFK + 4 * (j & 1);
         tc_cp_sf(sfk, smem_desc(sb + kOffKSF + ks * kSfAtomBytes, 0, 128, kSwizzleNone));
-        const uint32_t ka = sb + kOffK + ks * kTileBytes, qa = sb + kOffQ;
-        mma_mxf4(tmem + kColS + s * kTile, smem_desc(qa, 16, 512, kSwizzle64B), smem_desc(ka, 16, 512, kSwizzle64B),
-                 idesc_s0, tmem + kColSFQ, sfk, 0u);
-        mma_mxf4(tmem + kColS + s * kTile, smem_desc(qa + 32, 16, 512, kSwizzle64B),
-                 smem_desc(ka + 32, 16, 512, kSwizzle64B), idesc_s1, tmem + kColSFQ, sfk, 1u);
-        if (!((p.debug_flags & kDebugNeverArriveS) && j == 0)) tc_commit(bar(kBarSFull + s));
+        const uint32_t ka = sb + kOffK + ks * kTileBytes;
+        for (int g = 0; g < 2; g++) {
+          if (j >= (g ? ntiles1 : ntiles0)) continue;
+          // the single S buffer is free once the previous production was read
+          if (n >= 1 && !mbar_wait(bar(kBarSEmpty), (n - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = sb + kOffQ + g * kTileBytes, sfq = tmem + kColSFQ + 4 * g;
+          mma_mxf4(tmem + kColS, smem_desc(qa, 16, 512, kSwizzle64B), smem_desc(ka, 16, 512, kSwizzle64B), id0, sfq,
+                   sfk, 0u);
+          mma_mxf4(tmem + kColS, smem_desc(qa + 32, 16, 512, kSwizzle64B), smem_desc(ka + 32, 16, 512, kSwizzle64B),
+                   id1, sfq, sfk, 1u);
+          if (!((p.debug_flags & kDebugNeverArriveS) && n == 0)) tc_commit(bar(kBarSFull + g));
+          n++;
+        }
+        if (!ok) break;
         tc_commit(bar(kBarKEmpty + ks));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
-      if (ok && !issue_pv(T - 1)) ok = false;
+      if (!ok) record_error(p.status, 4, abort_flag);
+    }
+  } else if (warp == 2) {
+    // --------------------------------------------------------- PV issuer
+    if (lane == 0) {
+      const uint32_t id0 = idesc_mxf4(128, kPvN, 0, 0), id1 = idesc_mxf4(128, kPvN, 2, 2);
+      // scale atom of the ones rows, once into both V scale buffers
+      tc_cp_sf(tmem + kColSFV + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+      tc_cp_sf(tmem + kColSFV + 12, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+      bool ok = true;
+      for (int j = 0; ok && j < T; j++) {
+        const int vs = j % kVStages;
+        if (!mbar_wait(bar(kBarVFull + vs), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t va = sb + kOffV + vs * kVTileBytes, sfv = tmem + kColSFV + 8 * (j & 1);
+        bool sfv_loaded = false;
+        for (int g = 0; g < 2; g++) {
+          if (j >= (g ? ntiles1 : ntiles0)) continue;
+          if (!mbar_wait(bar(kBarPFull + g), j & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (!sfv_loaded) {
+            // the previous user of this buffer (tile j-2) is complete: the softmax
+            // threads waited for it before arriving on p_full
+            tc_cp_sf(sfv, smem_desc(sb + kOffVSF + vs * kSfAtomBytes, 0, 128, kSwizzleNone));
+            sfv_loaded = true;
+          }
+          const uint32_t pa = sb + kOffP + (2 * g + (j & 1)) * kTileBytes;
+          const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
+          const uint32_t od = tmem + kColO + g * kPvN;
+          mma_mxf4(od, smem_desc(pa, 16, 512, kSwizzle64B), smem_desc(va, 16, 512, kSwizzle64B), id0, sfp, sfv,
+                   j > 0 ? 1u : 0u);
+          mma_mxf4(od, smem_desc(pa + 32, 16, 512, kSwizzle64B), smem_desc(va + 32, 16, 512, kSwizzle64B), id1, sfp,
+                   sfv, 1u);
+          tc_commit(bar(kBarODone + g));
+          tc_commit(bar(kBarPEmpty + 2 * g + (j & 1)));
+        }
+        if (!ok) break;
+        tc_commit(bar(kBarVEmpty + vs));
+      }
       if (!ok) record_error(p.status, 4, abort_flag);
     }
   } else if (warp >= 4) {
     // --------------------------------------------------------- softmax
-    const int sw = warp - 4;
-    const int h = sw / 4;
+    const int g = (warp - 4) / 4;
     const int quad = warp % 4;
     const int r = quad * 32 + lane;
-    const int64_t qrow = static_cast<int64_t>(qt) * kTile + r;
+    const int Tg = g ? ntiles1 : ntiles0;
+    const int64_t qrow = static_cast<int64_t>(g ? qtile1 : qtile0) * kTile + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);
-    float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
-    float* lx = reinterpret_cast<float*>(smem + kOffLx);
-    float* pdiag = reinterpret_cast<float*>(smem + kOffPdiag);
+    const uint32_t ocol = kColO + g * kPvN;
     const float C = p.score_scale_log2;
-    const int ncols_o = h ? 72 : 64;  // O columns this half rescales (h=1 includes l at 128)
-    const uint32_t col_o0 = kColO + (h ? 64u : 0u);
     const bool ragged = (N % kTile) != 0;
     float m_run = -INFINITY;
     bool my_abort = false;
-    bool aborted = false;
+    uint32_t diag_words[4] = {0u, 0u, 0u, 0u};  // causal: P^ codes of the query's own 32-key block
+    uint32_t diag_sbyte = 127;
     // all lanes poll; the outcome is made warp-uniform so tcgen05 .sync.aligned ops stay convergent
     auto wait_uniform = [&](int b, uint32_t parity) {
       bool ok = !my_abort && mbar_wait(bar(b), parity, abort_flag);
@@ -312,205 +345,194 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    for (int j = 0; j < T; j++) {
-      const int s = j & 1;
-      float v[64];
-      wait_uniform(kBarSFull + s, (j >> 1) & 1);
+    for (int j = 0; j < Tg && !my_abort; j++) {
+      const int pb = j & 1;
+      float v[128];
+      wait_uniform(kBarSFull + g, j & 1);
+      if (my_abort) break;
       tc_fence_after();
-      if (!my_abort) {
-        uint32_t rr[32];
-        tmem_ld32(tl + kColS + s * kTile + 64 * h, rr);
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tl + kColS, r0);
+        tmem_ld32(tl + kColS + 32, r1);
+        tmem_ld32(tl + kColS + 64, r2);
+        tmem_ld32(tl + kColS + 96, r3);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(rr[i]);
-        tmem_ld32(tl + kColS + s * kTile + 64 * h + 32, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i++) v[32 + i] = __uint_as_float(rr[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; i++) v[i] = 0.0f;
+        for (int i = 0; i < 32; i++) {
+          v[i] = __uint_as_float(r0[i]);
+          v[32 + i] = __uint_as_float(r1[i]);
+          v[64 + i] = __uint_as_float(r2[i]);
+          v[96 + i] = __uint_as_float(r3[i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty + s));
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty));
 
-      const int64_t key0 = static_cast<int64_t>(j) * kTile + 64 * h;
-      if (j == T - 1 && (p.causal || ragged)) {
+      if (j == Tg - 1 && (p.causal || ragged)) {
+        const int64_t key0 = static_cast<int64_t>(j) * kTile;
 #pragma unroll
-        for (int i = 0; i < 64; i++) {
+        for (int i = 0; i < 128; i++) {
           const int64_t key = key0 + i;
-          const bool valid = key < N && (!p.causal || key <= qrow);
-          if (!valid) v[i] = -INFINITY;
+          if (!(key < N && (!p.causal || key <= qrow))) v[i] = -INFINITY;
         }
       }
-      float bm[2];
+      float bm[4];
 #pragma unroll
-      for (int b = 0; b < 2; b++) {
-        float m0 = v[32 * b];
-#pragma unroll
-        for (int i = 1; i < 31; i += 2) m0 = fmax3(m0, v[32 * b + i], v[32 * b + i + 1]);
-        bm[b] = fmaxf(m0, v[32 * b + 31]);
-      }
-      const float pm = fmaxf(bm[0], bm[1]);
-      xchg[(s * 2 + h) * kTile + r] = pm;
-      aborted = bar_red_or(1, 256, my_abort || *abort_flag);
-      if (aborted) break;
-      const float other = xchg[(s * 2 + (1 - h)) * kTile + r];
-      const float m_new = fmax3(m_run, pm, other);
+      for (int b = 0; b < 4; b++) bm[b] = max32(v + 32 * b);
+      const float m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
       const float mc = m_new * C;
 
-      // P^ = Q*(exp(S/sqrt(d) - m_new)) per 32-key block, scale from the block maximum
-      uint32_t words[8];
+      // the P^ buffer and its TMEM scale columns were last read by P^V^ of tile j-2
+      if (j >= 2) wait_uniform(kBarPEmpty + 2 * g + pb, ((j >> 1) - 1) & 1);
+      if (my_abort) break;
+      uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
+      const int swz = (r >> 1) & 3;
+      const bool diag_tile = p.causal && j == Tg - 1;
       uint32_t sbytes = 0;
 #pragma unroll
-      for (int b = 0; b < 2; b++) {
+      for (int b = 0; b < 4; b++) {
+        // P^ = Q*(exp(S/sqrt(d) - m_new)) for keys 32b..32b+31, scale from the block maximum
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
         uint32_t sbyte = 127;
-        if (bm[b] == -INFINITY) {
-#pragma unroll
-          for (int g = 0; g < 4; g++) words[4 * b + g] = 0u;
-        } else {
+        if (bm[b] != -INFINITY) {
           const float xb = fmaf(bm[b], C, -mc);
           int e = static_cast<int>(ceilf(xb - kLog2Qmax));
           e = e < -127 ? -127 : e;
           const float off = mc + static_cast<float>(e);
+          const float2 c2 = make_float2(C, C), noff2 = make_float2(-off, -off);
 #pragma unroll
-          for (int g = 0; g < 4; g++) {
+          for (int gq = 0; gq < 4; gq++) {
             float y[8];
 #pragma unroll
-            for (int i = 0; i < 8; i++) y[i] = ex2_approx(fmaf(v[32 * b + 8 * g + i], C, -off));
-            words[4 * b + g] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+            for (int i = 0; i < 8; i += 2) {
+              const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
+              y[i] = ex2_approx(x.x);
+              y[i + 1] = ex2_approx(x.y);
+            }
+            w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
           }
           sbyte = static_cast<uint32_t>(e + 127);
         }
         sbytes |= sbyte << (8 * b);
-      }
-      if (p.phat_codes != nullptr && qrow < N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.phat_codes + qrow * (static_cast<int64_t>(p.NT) * 64) +
-                                              static_cast<int64_t>(bh) * N * p.NT * 64 + j * 64 + 32 * h);
-        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-        *reinterpret_cast<uint16_t*>(p.phat_scales + (static_cast<int64_t>(bh) * N + qrow) * p.NT * 4 + j * 4 +
-                                     2 * h) = static_cast<uint16_t>(sbytes);
-      }
-      if (p.causal && j == qt && (quad >> 1) == h) {
-        // the query's own 32-key block: keep P^ for the bf16-V product, drop it from the MMA operand
-        const int lb = quad & 1;
-        const float sc = __uint_as_float(((sbytes >> (8 * lb)) & 0xFFu) << 23);  // 2^(byte-127)
-        float sum = 0.0f;
-#pragma unroll
-        for (int g = 0; g < 4; g++) {
-          const uint32_t w = lb ? words[4 + g] : words[g];
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const float val = e2m1_decode((w >> (4 * i)) & 0xFu) * sc;
-            pdiag[r * kPdiagStride + 8 * g + i] = val;
-            sum += val;
-          }
-          if (lb) words[4 + g] = 0u; else words[g] = 0u;
+        if (p.phat_codes != nullptr && qrow < N) {
+          *reinterpret_cast<uint4*>(p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64 + 16 * b) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
-        lx[r] = sum;
+        if (diag_tile && b == quad) {
+          // the query's own 32-key block: keep its codes for the bf16-V product,
+          // drop it from the tensor-core operand
+#pragma unroll
+          for (int gq = 0; gq < 4; gq++) {
+            diag_words[gq] = w[gq];
+            w[gq] = 0u;
+          }
+          diag_sbyte = sbyte;
+        }
+        *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      if (j >= 2) wait_uniform(kBarPEmpty + s, ((j >> 1) - 1) & 1);
-      {
-        // P^ tile (128 rows x 64 bytes, 64-byte swizzle): this half owns 16-byte chunks 2h, 2h+1
-        uint8_t* prow = smem + kOffP + s * kTileBytes + r * 64;
-        const int x = (r >> 1) & 3;
-        *reinterpret_cast<uint4*>(prow + (((2 * h) ^ x) << 4)) = make_uint4(words[0], words[1], words[2], words[3]);
-        *reinterpret_cast<uint4*>(prow + (((2 * h + 1) ^ x) << 4)) = make_uint4(words[4], words[5], words[6], words[7]);
-        *reinterpret_cast<uint16_t*>(smem + kOffPSF + s * kSfAtomBytes + (r % 32) * 16 + (r / 32) * 4 + 2 * h) =
-            static_cast<uint16_t>(sbytes);
-      }
+      if (p.phat_codes != nullptr && qrow < N)
+        *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
+      // P^ scales: lane r, column base + r/32 of this group's scale buffer
+      tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
       fence_proxy_async_smem();
-      const float alpha = (j == 0) ? 0.0f : ex2_approx((m_run - m_new) * C);
+      tmem_wait_st();
       if (j >= 1) {
-        wait_uniform(kBarODone, (j - 1) & 1);
+        // O_g is stable once P^V^ of tile j-1 completes; rescale by alpha if any row's max moved
+        const float alpha = ex2_approx((m_run - m_new) * C);
+        wait_uniform(kBarODone + g, (j - 1) & 1);
+        if (my_abort) break;
         tc_fence_after();
-        if (!my_abort && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          for (int c0 = 0; c0 < ncols_o; c0 += 8) {
-            uint32_t o[8];
-            tmem_ld8(tl + col_o0 + c0, o);
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            uint32_t o[32];
+            tmem_ld32(tl + ocol + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 8; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st8(tl + col_o0 + c0, o);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+              o[i] = __float_as_uint(x.x);
+              o[i + 1] = __float_as_uint(x.y);
+            }
+            tmem_st32(tl + ocol + 32 * c, o);
           }
+          const uint32_t l = tmem_ld1(tl + ocol + kD);
+          tmem_wait_ld();
+          tmem_st1(tl + ocol + kD, __float_as_uint(__uint_as_float(l) * alpha));
           tmem_wait_st();
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + s));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + g));
       m_run = m_new;
     }
 
     // --------------------------------------------------------- epilogue
-    if (!aborted) wait_uniform(kBarODone, (T - 1) & 1);
-    tc_fence_after();
-    __nv_bfloat16* vdiag = reinterpret_cast<__nv_bfloat16*>(smem + kOffVdiag);
-    if (p.causal) {
-      // bf16 V rows of the diagonal key tile (keys >= N read as 0)
-      const int t = threadIdx.x - 128;
-      const uint4* src = reinterpret_cast<const uint4*>(p.v_bf16 + (static_cast<int64_t>(bh) * N) * kD);
-      for (int i = t; i < kTile * 16; i += 256) {
-        const int row = i / 16;
-        const int64_t key = static_cast<int64_t>(qt) * kTile + row;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (key < N) val = src[key * 16 + (i % 16)];
-        reinterpret_cast<uint4*>(vdiag)[i] = val;
-      }
-    }
-    if (h == 1) {
-      float l = 0.0f;
-      if (!my_abort && !aborted) {
-        uint32_t o[8];
-        tmem_ld8(tl + kColO + kD, o);
+    if (Tg > 0) {
+      wait_uniform(kBarODone + g, (Tg - 1) & 1);
+      tc_fence_after();
+      if (!my_abort) {
+        float l = __uint_as_float(tmem_ld1(tl + ocol + kD));
         tmem_wait_ld();
-        l = __uint_as_float(o[0]);
-      }
-      if (p.causal) l += lx[r];
-      lsum[r] = l;
-    }
-    named_bar_sync(2, 256);
-    const float inv_l = 1.0f / lsum[r];
-    if (!my_abort && !aborted) {
-      float acc[64];
-      uint32_t rr[32];
-      tmem_ld32(tl + kColO + 64 * h, rr);
-      tmem_wait_ld();
+        float dv[32];
+        const bool diag = p.causal != 0;
+        if (diag) {
+          const float sc = __uint_as_float(diag_sbyte << 23);  // 2^(byte-127)
 #pragma unroll
-      for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(rr[i]);
-      tmem_ld32(tl + kColO + 64 * h + 32, rr);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; i++) acc[32 + i] = __uint_as_float(rr[i]);
-      if (p.causal) {
-        const int kq = quad * 32;  // first key (within the diagonal tile) of this row's 32-token block
-        for (int k = 0; k < 32; k++) {
-          const float pk = pdiag[r * kPdiagStride + k];
-          if (pk == 0.0f) continue;
-          const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(vdiag + (kq + k) * kD + 64 * h);
-#pragma unroll
-          for (int i = 0; i < 32; i++) {
-            const float2 f = __bfloat1622float2(vr[i]);
-            acc[2 * i] = fmaf(pk, f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(pk, f.y, acc[2 * i + 1]);
+          for (int k = 0; k < 32; k++) {
+            dv[k] = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * sc;
+            l += dv[k];
           }
         }
-      }
-      if (qrow < N) {
-        float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + qrow) * kD + 64 * h);
+        const float inv_l = 1.0f / l;
+        // keys of the diagonal block: tile Tg-1, rows 32*quad .. 32*quad+31
+        const int64_t dkey0 = static_cast<int64_t>(Tg - 1) * kTile + 32 * quad;
+        const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_bf16);
+#pragma unroll 1
+        for (int c = 0; c < 4; c++) {
+          uint32_t o[32];
+          tmem_ld32(tl + ocol + 32 * c, o);
+          tmem_wait_ld();
+          float acc[32];
 #pragma unroll
-        for (int i = 0; i < 16; i++)
-          dst[i] = make_float4(acc[4 * i] * inv_l, acc[4 * i + 1] * inv_l, acc[4 * i + 2] * inv_l,
-                               acc[4 * i + 3] * inv_l);
+          for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
+          if (diag) {
+#pragma unroll
+            for (int k = 0; k < 32; k++) {
+              const int64_t key = dkey0 + k;
+              if (dv[k] == 0.0f || key >= N) continue;
+              const uint4* row = vsrc + ((static_cast<int64_t>(bh) * N + key) * kD + 32 * c) / 8;
+#pragma unroll
+              for (int q4 = 0; q4 < 4; q4++) {
+                const uint4 u = __ldg(row + q4);
+                const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int t2 = 0; t2 < 4; t2++) {
+                  acc[8 * q4 + 2 * t2] = fmaf(dv[k], __uint_as_float(uu[t2] << 16), acc[8 * q4 + 2 * t2]);
+                  acc[8 * q4 + 2 * t2 + 1] = fmaf(dv[k], __uint_as_float(uu[t2] & 0xFFFF0000u), acc[8 * q4 + 2 * t2 + 1]);
+                }
+              }
+            }
+          }
+          if (qrow < N) {
+            float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + qrow) * kD + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+              dst[i] = make_float4(acc[4 * i] * inv_l, acc[4 * i + 1] * inv_l, acc[4 * i + 2] * inv_l,
+                                   acc[4 * i + 3] * inv_l);
+          }
+        }
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -550,13 +572,17 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.causal = a.causal;
   p.debug_flags = a.debug_flags;
   p.score_scale_log2 = kLog2e / 11.313708498984761f;  // log2(e) / sqrt(128)
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mxfp4_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(mxfp4_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
+  dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
   mxfp4_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
