@@ -73,8 +73,7 @@ constexpr int kBarVEmpty = kBarVFull + kVStages;
 constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2 groups]: S holds S_g of the next tile
 constexpr int kBarSEmpty = kBarSFull + 2;         // 4 arrivals: the S buffer was read
 constexpr int kBarPFull = kBarSEmpty + 1;         // [2 groups], 4 arrivals: P^ tile + O rescale ready
-constexpr int kBarPEmpty = kBarPFull + 2;         // [2 groups][2 buffers]: P^ buffer free
-constexpr int kBarODone = kBarPEmpty + 4;         // [2 groups]: P^V^ into O_g complete
+constexpr int kBarODone = kBarPFull + 2;          // [2 groups]: P^V^ into O_g complete
 static_assert(kBarODone + 2 <= kNumBars, "barrier space");
 
 // TMEM columns
@@ -173,8 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + g), 1);
       mbar_init(bar(kBarPFull + g), 4);
       mbar_init(bar(kBarODone + g), 1);
-      mbar_init(bar(kBarPEmpty + 2 * g), 1);
-      mbar_init(bar(kBarPEmpty + 2 * g + 1), 1);
     }
     mbar_init(bar(kBarSEmpty), 4);
     fence_mbar_init();
@@ -199,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
-
+  if (warp < 4) {
   if (warp == 0) {
     // --------------------------------------------------------- producer
     if (lane == 0) {
@@ -313,14 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_mxf4(od, smem_desc(pa + 32, 16, 512, kSwizzle64B), smem_desc(va + 32, 16, 512, kSwizzle64B), id1, sfp,
                    sfv, 1u);
           tc_commit(bar(kBarODone + g));
-          tc_commit(bar(kBarPEmpty + 2 * g + (j & 1)));
         }
         if (!ok) break;
         tc_commit(bar(kBarVEmpty + vs));
       }
       if (!ok) record_error(p.status, 4, abort_flag);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
     // --------------------------------------------------------- softmax
     const int g = (warp - 4) / 4;
     const int quad = warp % 4;
@@ -358,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + kColS + 64, r2);
         tmem_ld32(tl + kColS + 96, r3);
         tmem_wait_ld();
+        reg_fence32(r0);
+        reg_fence32(r1);
+        reg_fence32(r2);
+        reg_fence32(r3);
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           v[i] = __uint_as_float(r0[i]);
@@ -371,12 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kBarSEmpty));
 
       if (j == Tg - 1 && (p.causal || ragged)) {
+        // keys of this tile visible to the row: i < nvalid (key < N, and key <= row if causal)
         const int64_t key0 = static_cast<int64_t>(j) * kTile;
+        int64_t lim = N - key0;
+        if (p.causal && qrow + 1 - key0 < lim) lim = qrow + 1 - key0;
+        const int nvalid = lim < 0 ? 0 : (lim > kTile ? kTile : static_cast<int>(lim));
 #pragma unroll
-        for (int i = 0; i < 128; i++) {
-          const int64_t key = key0 + i;
-          if (!(key < N && (!p.causal || key <= qrow))) v[i] = -INFINITY;
-        }
+        for (int i = 0; i < 128; i++) v[i] = (i < nvalid) ? v[i] : -INFINITY;
       }
       float bm[4];
 #pragma unroll
@@ -384,42 +386,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
       const float mc = m_new * C;
 
-      // the P^ buffer and its TMEM scale columns were last read by P^V^ of tile j-2
-      if (j >= 2) wait_uniform(kBarPEmpty + 2 * g + pb, ((j >> 1) - 1) & 1);
-      if (my_abort) break;
+      // The P^ buffer and TMEM scale columns of parity pb were last read by P^V^ of
+      // tile j-2; this thread saw that product complete in its o_done wait of tile j-1.
+      // P^ = Q*(exp(S/sqrt(d) - m_new)) per 32-key block with the UOS scale of the
+      // block maximum. Branch-free: a fully masked block has max -inf, all its
+      // exponentials are 0 and it takes the all-zero-block scale (byte 127).
       uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
       const int swz = (r >> 1) & 3;
       const bool diag_tile = p.causal && j == Tg - 1;
+      uint8_t* dump = (p.phat_codes != nullptr && qrow < N)
+                          ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
+                          : nullptr;
+      const float2 c2 = make_float2(C, C);
       uint32_t sbytes = 0;
 #pragma unroll
       for (int b = 0; b < 4; b++) {
-        // P^ = Q*(exp(S/sqrt(d) - m_new)) for keys 32b..32b+31, scale from the block maximum
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        uint32_t sbyte = 127;
-        if (bm[b] != -INFINITY) {
-          const float xb = fmaf(bm[b], C, -mc);
-          int e = static_cast<int>(ceilf(xb - kLog2Qmax));
-          e = e < -127 ? -127 : e;
-          const float off = mc + static_cast<float>(e);
-          const float2 c2 = make_float2(C, C), noff2 = make_float2(-off, -off);
-#pragma unroll
-          for (int gq = 0; gq < 4; gq++) {
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
-              y[i] = ex2_approx(x.x);
-              y[i + 1] = ex2_approx(x.y);
-            }
-            w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-          }
-          sbyte = static_cast<uint32_t>(e + 127);
-        }
+        const bool empty = bm[b] == -INFINITY;
+        const float xb = fmaf(bm[b], C, -mc);
+        int e = static_cast<int>(ceilf(xb - kLog2Qmax));
+        e = empty ? -127 : (e < -127 ? -127 : e);
+        const float off = mc + static_cast<float>(e);
+        const uint32_t sbyte = empty ? 127u : static_cast<uint32_t>(e + 127);
         sbytes |= sbyte << (8 * b);
-        if (p.phat_codes != nullptr && qrow < N) {
-          *reinterpret_cast<uint4*>(p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64 + 16 * b) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        const float2 noff2 = make_float2(-off, -off);
+        uint32_t w[4];
+#pragma unroll
+        for (int gq = 0; gq < 4; gq++) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
+            y[i] = ex2_approx(x.x);
+            y[i + 1] = ex2_approx(x.y);
+          }
+          w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
         }
+        if (dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
         if (diag_tile && b == quad) {
           // the query's own 32-key block: keep its codes for the bf16-V product,
           // drop it from the tensor-core operand
@@ -432,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      if (p.phat_codes != nullptr && qrow < N)
+      if (dump != nullptr)
         *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
       // P^ scales: lane r, column base + r/32 of this group's scale buffer
       tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
@@ -445,22 +447,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (my_abort) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          // O_g row (128 columns + l) *= alpha: all loads in flight at once, one wait
           const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < 4; c++) {
-            uint32_t o[32];
-            tmem_ld32(tl + ocol + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 x = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-              o[i] = __float_as_uint(x.x);
-              o[i + 1] = __float_as_uint(x.y);
-            }
-            tmem_st32(tl + ocol + 32 * c, o);
-          }
-          const uint32_t l = tmem_ld1(tl + ocol + kD);
+          uint32_t o0[32], o1[32], o2[32], o3[32];
+          tmem_ld32(tl + ocol, o0);
+          tmem_ld32(tl + ocol + 32, o1);
+          tmem_ld32(tl + ocol + 64, o2);
+          tmem_ld32(tl + ocol + 96, o3);
+          uint32_t l = tmem_ld1(tl + ocol + kD);
           tmem_wait_ld();
+          reg_fence32(o0);
+          reg_fence32(o1);
+          reg_fence32(o2);
+          reg_fence32(o3);
+          reg_fence1(l);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float2 x;
+            x = __fmul2_rn(make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), a2);
+            o0[i] = __float_as_uint(x.x);
+            o0[i + 1] = __float_as_uint(x.y);
+            x = __fmul2_rn(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), a2);
+            o1[i] = __float_as_uint(x.x);
+            o1[i + 1] = __float_as_uint(x.y);
+            x = __fmul2_rn(make_float2(__uint_as_float(o2[i]), __uint_as_float(o2[i + 1])), a2);
+            o2[i] = __float_as_uint(x.x);
+            o2[i + 1] = __float_as_uint(x.y);
+            x = __fmul2_rn(make_float2(__uint_as_float(o3[i]), __uint_as_float(o3[i + 1])), a2);
+            o3[i] = __float_as_uint(x.x);
+            o3[i + 1] = __float_as_uint(x.y);
+          }
+          tmem_st32(tl + ocol, o0);
+          tmem_st32(tl + ocol + 32, o1);
+          tmem_st32(tl + ocol + 64, o2);
+          tmem_st32(tl + ocol + 96, o3);
           tmem_st1(tl + ocol + kD, __float_as_uint(__uint_as_float(l) * alpha));
           tmem_wait_st();
         }
@@ -476,17 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_uniform(kBarODone + g, (Tg - 1) & 1);
       tc_fence_after();
       if (!my_abort) {
-        float l = __uint_as_float(tmem_ld1(tl + ocol + kD));
+        uint32_t lbits = tmem_ld1(tl + ocol + kD);
         tmem_wait_ld();
-        float dv[32];
+        reg_fence1(lbits);
+        float l = __uint_as_float(lbits);
         const bool diag = p.causal != 0;
+        const float dsc = __uint_as_float(diag_sbyte << 23);  // 2^(byte-127)
         if (diag) {
-          const float sc = __uint_as_float(diag_sbyte << 23);  // 2^(byte-127)
 #pragma unroll
-          for (int k = 0; k < 32; k++) {
-            dv[k] = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * sc;
-            l += dv[k];
-          }
+          for (int k = 0; k < 32; k++) l += e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
         }
         const float inv_l = 1.0f / l;
         // keys of the diagonal block: tile Tg-1, rows 32*quad .. 32*quad+31
@@ -497,14 +515,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld32(tl + ocol + 32 * c, o);
           tmem_wait_ld();
+          reg_fence32(o);
           float acc[32];
 #pragma unroll
           for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
           if (diag) {
-#pragma unroll
+#pragma unroll 1
             for (int k = 0; k < 32; k++) {
+              const uint32_t wk = k < 8 ? diag_words[0] : (k < 16 ? diag_words[1] : (k < 24 ? diag_words[2] : diag_words[3]));
+              const float pk = e2m1_decode((wk >> (4 * (k & 7))) & 0xFu) * dsc;
               const int64_t key = dkey0 + k;
-              if (dv[k] == 0.0f || key >= N) continue;
+              if (pk == 0.0f || key >= N) continue;
               const uint4* row = vsrc + ((static_cast<int64_t>(bh) * N + key) * kD + 32 * c) / 8;
 #pragma unroll
               for (int q4 = 0; q4 < 4; q4++) {
@@ -512,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int t2 = 0; t2 < 4; t2++) {
-                  acc[8 * q4 + 2 * t2] = fmaf(dv[k], __uint_as_float(uu[t2] << 16), acc[8 * q4 + 2 * t2]);
-                  acc[8 * q4 + 2 * t2 + 1] = fmaf(dv[k], __uint_as_float(uu[t2] & 0xFFFF0000u), acc[8 * q4 + 2 * t2 + 1]);
+                  acc[8 * q4 + 2 * t2] = fmaf(pk, __uint_as_float(uu[t2] << 16), acc[8 * q4 + 2 * t2]);
+                  acc[8 * q4 + 2 * t2 + 1] = fmaf(pk, __uint_as_float(uu[t2] & 0xFFFF0000u), acc[8 * q4 + 2 * t2 + 1]);
                 }
               }
             }
