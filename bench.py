@@ -109,38 +109,43 @@ def _dist():
 
 
 def cpu_oracle_sample(w, budget_rows: int, seed: int = 0):
-    """Time the oracle on a bounded sample of workload `w`: one head's K and V
-    quantized in full plus `budget_rows` query rows through the forward.
-    Returns (seconds, flops, description, threads)."""
+    """Time the oracle on a bounded sample of workload `w`: per sampled head, its
+    K and V quantized in full plus up to N query rows through the forward, over
+    as many heads as `budget_rows` needs. Returns (seconds, flops, description,
+    threads)."""
     import numpy as np
-    import torch
 
     import oracle
     from mxfp4_precision_attention_gb300 import workloads as W
 
     oracle.build()
-    q, k, v = W.generate(w, device="cpu", B=1, H=1, seed=w.seed + seed)
-    qb, kb, vb = (W.as_u16(t).reshape(1, w.N, 128) for t in (q, k, v))
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(w.N, size=min(budget_rows, w.N), replace=False))
-    t0 = time.perf_counter()
-    qc, qs = oracle.rotate_quantize_qk(qb[:, toks])
-    kc, ks = oracle.rotate_quantize_qk(kb)
-    vc, vs = oracle.quantize_v(vb)
-    # the forward needs Q codes at the sampled token positions
-    qc_full = np.zeros((1, w.N, 128), dtype=np.uint8)
-    qs_full = np.full((1, w.N, 4), 127, dtype=np.uint8)
-    qc_full[:, toks], qs_full[:, toks] = qc, qs
-    rows = np.stack([np.zeros_like(toks), toks], axis=1)
-    oracle.forward(qc_full, qs_full, kc, ks, vc, vs, rows, vraw_u16=vb, causal=w.causal)
-    dt = time.perf_counter() - t0
-    if w.causal:
-        flops = float(sum(4.0 * (int(t) + 1) * 128 for t in toks))
-    else:
-        flops = 4.0 * len(toks) * w.N * 128
-    desc = (f"1 head of {w.name}: rotate+quantize {len(toks)} Q rows and all {w.N} K tokens, quantize all V, "
-            f"float64 forward for {len(toks)} query rows against all keys")
-    del torch
+    rows_left = max(1, int(budget_rows))
+    nheads = (rows_left + w.N - 1) // w.N
+    dt, flops, rows_done = 0.0, 0.0, 0
+    for hh in range(nheads):
+        q, k, v = W.generate(w, device="cpu", B=1, H=1, seed=w.seed + 1000 * seed + hh)
+        qb, kb, vb = (W.as_u16(t).reshape(1, w.N, 128) for t in (q, k, v))
+        rng = np.random.default_rng(seed * 7919 + hh)
+        nr = min(rows_left, w.N)
+        toks = np.sort(rng.choice(w.N, size=nr, replace=False))
+        t0 = time.perf_counter()
+        qc, qs = oracle.rotate_quantize_qk(qb[:, toks])
+        kc, ks = oracle.rotate_quantize_qk(kb)
+        vc, vs = oracle.quantize_v(vb)
+        qc_full = np.zeros((1, w.N, 128), dtype=np.uint8)
+        qs_full = np.full((1, w.N, 4), 127, dtype=np.uint8)
+        qc_full[:, toks], qs_full[:, toks] = qc, qs
+        rows = np.stack([np.zeros_like(toks), toks], axis=1)
+        oracle.forward(qc_full, qs_full, kc, ks, vc, vs, rows, vraw_u16=vb, causal=w.causal)
+        dt += time.perf_counter() - t0
+        if w.causal:
+            flops += float(sum(4.0 * (int(t) + 1) * 128 for t in toks))
+        else:
+            flops += 4.0 * len(toks) * w.N * 128
+        rows_left -= nr
+        rows_done += nr
+    desc = (f"{nheads} head(s) of {w.name}: per head rotate+quantize the sampled Q rows and all {w.N} K tokens, "
+            f"quantize all V, float64 forward for the sampled rows against all keys ({rows_done} rows in total)")
     return dt, flops, desc, oracle.num_threads()
 
 
@@ -149,9 +154,9 @@ def run_reference(args, w):
     if rank != 0:
         return
     # calibrate the sample so that one step costs ~ args.ref_step_s seconds
-    dt, fl, _, _ = cpu_oracle_sample(w, 8)
-    per_row = max(dt / 8, 1e-4)
-    rows = int(max(8, min(4096, args.ref_step_s / per_row)))
+    dt, fl, _, _ = cpu_oracle_sample(w, 256)
+    per_row = max(dt / 256, 1e-6)
+    rows = int(max(8, min(200000, args.ref_step_s / per_row)))
     for i in range(args.warmup):
         cpu_oracle_sample(w, max(4, rows // 8), seed=100 + i)
     times, flops = [], []
@@ -282,8 +287,8 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        dt0, _, _, _ = cpu_oracle_sample(w, 4)
-        rows = int(max(8, min(2048, args.cpu_budget_s / max(dt0 / 4, 1e-4))))
+        dt0, _, _, _ = cpu_oracle_sample(w, 256)
+        rows = int(max(8, min(200000, args.cpu_budget_s / max(dt0 / 256, 1e-6))))
         dt, fl, desc, thr = cpu_oracle_sample(w, rows, seed=1)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
                "seconds": dt}

@@ -132,6 +132,9 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
   atomicCAS(status, 0, code);
 }
 
+// kCausal and kDump are compile-time so the non-causal, non-diagnostic path
+// carries no checks for either.
+template <bool kCausal, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -148,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.y;
   const int npairs = (p.NT + 1) / 2;
   // causal: heaviest query tiles first
-  const int pair = p.causal ? (npairs - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int pair = kCausal ? (npairs - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int qtile0 = 2 * pair, qtile1 = 2 * pair + 1;
   const bool has_b = qtile1 < p.NT;
-  const int ntiles0 = p.causal ? qtile0 + 1 : p.NT;
-  const int ntiles1 = has_b ? (p.causal ? qtile1 + 1 : p.NT) : 0;
+  const int ntiles0 = kCausal ? qtile0 + 1 : p.NT;
+  const int ntiles1 = has_b ? (kCausal ? qtile1 + 1 : p.NT) : 0;
   const int T = ntiles0 > ntiles1 ? ntiles0 : ntiles1;  // key tiles streamed by this CTA
   const int64_t N = p.N;
 
@@ -371,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty));
 
-      if (j == Tg - 1 && (p.causal || ragged)) {
+      if (j == Tg - 1 && (kCausal || ragged)) {
         // keys of this tile visible to the row: i < nvalid (key < N, and key <= row if causal)
         const int64_t key0 = static_cast<int64_t>(j) * kTile;
         int64_t lim = N - key0;
-        if (p.causal && qrow + 1 - key0 < lim) lim = qrow + 1 - key0;
+        if (kCausal && qrow + 1 - key0 < lim) lim = qrow + 1 - key0;
         const int nvalid = lim < 0 ? 0 : (lim > kTile ? kTile : static_cast<int>(lim));
 #pragma unroll
         for (int i = 0; i < 128; i++) v[i] = (i < nvalid) ? v[i] : -INFINITY;
@@ -393,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // exponentials are 0 and it takes the all-zero-block scale (byte 127).
       uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
       const int swz = (r >> 1) & 3;
-      const bool diag_tile = p.causal && j == Tg - 1;
-      uint8_t* dump = (p.phat_codes != nullptr && qrow < N)
+      const bool diag_tile = kCausal && j == Tg - 1;
+      uint8_t* dump = (kDump && qrow < N)
                           ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
                           : nullptr;
       const float2 c2 = make_float2(C, C);
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
         }
-        if (dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
         if (diag_tile && b == quad) {
           // the query's own 32-key block: keep its codes for the bf16-V product,
           // drop it from the tensor-core operand
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      if (dump != nullptr)
+      if (kDump && dump != nullptr)
         *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
       // P^ scales: lane r, column base + r/32 of this group's scale buffer
       tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence1(lbits);
         float l = __uint_as_float(lbits);
-        const bool diag = p.causal != 0;
+        const bool diag = kCausal;
         const float dsc = __uint_as_float(diag_sbyte << 23);  // 2^(byte-127)
         if (diag) {
 #pragma unroll
@@ -599,12 +602,22 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   static bool attr_set[64] = {false};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(mxfp4_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {mxfp4_fwd_kernel<false, false>, mxfp4_fwd_kernel<true, false>, mxfp4_fwd_kernel<false, true>,
+                    mxfp4_fwd_kernel<true, true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
-  mxfp4_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  const bool dump = a.phat_codes != nullptr;
+  if (a.causal) {
+    if (dump) mxfp4_fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  } else {
+    if (dump) mxfp4_fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  }
   return cudaGetLastError();
 }
 
