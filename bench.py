@@ -35,6 +35,41 @@ UNIT = "TFLOPS"
 FP4_OVER_BF16_NOMINAL = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rate on GB300
 
 
+# DRAM bytes of one forward launch from an ncu capture (dram__bytes_read.sum,
+# dram__bytes_write.sum), with the B*H and N it was taken at and a fingerprint
+# of the kernel source it was taken on. `traffic` is reported (scaled by B*H)
+# only while the source still has that fingerprint; otherwise it is null.
+FWD_TRAFFIC_CAPTURE = {
+    "fingerprint": "389a5249f5a4fc44",
+    "bh": 8, "n": 32760,
+    "read_bytes": 53530624, "write_bytes": 79385856,
+}
+FWD_SOURCES = ("attn_mxfp4.cu", "sm103_ptx.cuh", "internal.h")
+
+
+def kernel_fingerprint() -> str:
+    """sha256 of the forward kernel's sources with comments and blank space removed."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for name in FWD_SOURCES:
+        with open(os.path.join(ROOT, "mxfp4_precision_attention_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(name.encode())
+        h.update(" ".join(src.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def fwd_traffic(bh: int, n: int):
+    c = FWD_TRAFFIC_CAPTURE
+    if c["fingerprint"] != kernel_fingerprint() or n != c["n"]:
+        return None
+    return (c["read_bytes"] + c["write_bytes"]) * bh / c["bh"]
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -297,13 +332,14 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, ue8m0 scales, fp32 accumulate)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4",
             "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": 128, "causal": w.causal,
                        "parallelism": f"replicas x{world} (heads shard, no collective)",
                        "l2": f"inputs {3 * e * 2 / 1e9:.2f} GB per step vs 129 MB L2; no flush"},
             "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
-                         "frac": fwd_tflops / fp4_peak, "traffic": None,
+                         "frac": fwd_tflops / fp4_peak, "traffic": fwd_traffic(B * H, N),
+                         "traffic_note": "DRAM bytes per launch, scaled by B*H from an 8-head ncu capture of the same kernel source",
                          "kernel": "mxfp4_fwd_kernel",
                          "peak_source": f"{peak_src} bf16 {bf16:.1f} TF/s x nominal fp4/bf16 ratio {FP4_OVER_BF16_NOMINAL:g}"},
             "breakdown_ms": {"rotate_quantize_qk_x2": qk_ms, "quantize_v": v_ms, "forward": fwd_ms},

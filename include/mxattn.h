@@ -70,7 +70,7 @@ MXATTN_API size_t mxattn_qk_scales_bytes(int64_t B, int64_t H, int64_t N); /* B*
 MXATTN_API size_t mxattn_v_codes_bytes(int64_t B, int64_t H, int64_t N);   /* B*H*128*Npad/2 */
 MXATTN_API size_t mxattn_v_scales_bytes(int64_t B, int64_t H, int64_t N);  /* B*H*ceil(N/128)*512 */
 
-/* Algorithm 2 lines 3-6 (with Algorithm 1): rotate every token of x by the
+/* Algorithm 2 (section 4.3), rotation and Q/K quantization, with Algorithm 1: rotate every token of x by the
  * fixed Hadamard matrix R_H = H_128/sqrt(128) (Sylvester order, binary32
  * butterflies h = 1..64 then one multiply by the binary32 nearest 2^-3.5) and
  * quantize each 32-channel block with the UOS scale.
@@ -81,7 +81,7 @@ MXATTN_API size_t mxattn_v_scales_bytes(int64_t B, int64_t H, int64_t N);  /* B*
 MXATTN_API mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
                                         void* scales, void* stream);
 
-/* Algorithm 2 line 7: quantize V in blocks of 32 consecutive tokens per
+/* Algorithm 2 (section 4.3), V quantization: quantize V in blocks of 32 consecutive tokens per
  * channel (blocks counted from token 0; the last block is zero padded) with
  * the UOS scale; codes are written channel-major (see layouts above).
  *   v      : bf16 [B, H, N, 128] (device, read only)
@@ -89,7 +89,7 @@ MXATTN_API mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int
 MXATTN_API mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
                                 void* scales, void* stream);
 
-/* Algorithm 2 lines 8-21 on quantized operands: for every query row, key
+/* Algorithm 2 (section 4.3), the attention loop, on quantized operands: for every query row, key
  * tiles of Bc = 128 in increasing order; S = Q^K^T/sqrt(d) and P^V^ on
  * tcgen05 block-scaled MXFP4 tensor cores; running max m, rescale
  * alpha = exp(m_old - m_new); P~ = exp(S - m_new) quantized per 32-key block

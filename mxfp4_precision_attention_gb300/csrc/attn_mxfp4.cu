@@ -1,5 +1,5 @@
 // MXFP4 fused attention forward with Pre-Normalization Quantization
-// ("MXAttention", Algorithm 2 lines 8-21; Eqs. 2-8 and 44-48).
+// ("MXAttention", Algorithm 2 in section 4.3; Eqs. 2-8 and 44-48).
 //
 // Per query row, key tiles of Bc = 128 in increasing order:
 //   S_j   = Q^ K^_j^T                 tcgen05.mma kind::mxf4 block_scale -> TMEM

@@ -1,5 +1,6 @@
-// MXFP4 quantizers of the MXAttention forward ("MXAttention", Algorithm 2
-// lines 3-7, with the UOS block quantizer of Algorithm 1).
+// MXFP4 quantizers of the MXAttention forward ("MXAttention", the rotation
+// and quantization steps of Algorithm 2 in section 4.3, with the UOS block
+// quantizer of Algorithm 1).
 //
 //  (a) rotate_quantize_qk: per token, Hadamard-rotate the 128 channels
 //      (binary32 butterflies h = 1,2,...,64, then x 2^-3.5 rounded to binary32)

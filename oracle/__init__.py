@@ -129,7 +129,7 @@ def hadamard_fp32(x_u16: np.ndarray) -> np.ndarray:
 
 
 def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True):
-    """Alg. 2 lines 3-6. ``x_u16``: bf16 bits ``[..., 128]``.
+    """Algorithm 2 (section 4.3), the rotation and Q/K quantization steps. ``x_u16``: bf16 bits ``[..., 128]``.
 
     Returns (codes ``[..., 128]`` uint8, scales ``[..., 4]`` uint8)."""
     lib = _load()
@@ -143,7 +143,7 @@ def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True):
 
 
 def quantize_v(v_u16: np.ndarray, rule: int = UOS):
-    """Alg. 2 line 7 on ``[BH, N, 128]`` bf16 bits.
+    """Algorithm 2 (section 4.3), the V quantization step, on ``[BH, N, 128]`` bf16 bits.
 
     Returns (codes ``[BH, N, 128]``, scales ``[BH, 128, ceil(N/32)]``)."""
     lib = _load()
@@ -158,7 +158,7 @@ def quantize_v(v_u16: np.ndarray, rule: int = UOS):
 
 def online_softmax(q_rows, row_tok, K, V, Vraw=None, *, causal=False, quant_p=True, placement=PNQ,
                    p_rule=UOS, bc=BC, want_phat=False):
-    """Alg. 2 lines 8-20 on real-valued inputs (float64).
+    """Algorithm 2 (section 4.3), the tiled online-softmax loop (Eqs. 2-8, 44-48), on real-valued inputs (float64).
 
     ``q_rows``: ``[R, 128]``; ``row_tok``: token index of each row; ``K, V``:
     ``[N, 128]``. Returns dict with ``out``, ``ell`` and optionally ``phat``

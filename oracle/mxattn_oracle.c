@@ -138,7 +138,7 @@ void orc_hadamard_fp32(const uint16_t* x_bf16, float* y) {
 }
 
 /* ------------------------------------------------- Q / K quantization
- * Alg. 2 lines 3-6: rotate each token, then quantize each 32-channel block.
+ * Algorithm 2 (section 4.3), Q/K steps: rotate each token, then quantize each 32-channel block.
  * codes: rows x 128 (one code per byte); scales: rows x 4 biased bytes.    */
 void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotate, uint8_t* codes,
                             uint8_t* scales) {
@@ -159,7 +159,7 @@ void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotat
 }
 
 /* ---------------------------------------------------- V quantization
- * Alg. 2 line 7 with token blocks (R4). v: [BH][N][128] bf16.
+ * Algorithm 2 (section 4.3), V step, with token blocks (R4). v: [BH][N][128] bf16.
  * codes: [BH][N][128] (token-major, one code per byte);
  * scales: [BH][128][nblk], nblk = ceil(N/32).                              */
 void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, uint8_t* codes, uint8_t* scales) {
@@ -181,7 +181,7 @@ void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, uint8_t*
 }
 
 /* ------------------------------------------------ online softmax core
- * Alg. 2 lines 8-20 for one query row against one head's keys, float64.
+ * Algorithm 2 (section 4.3) loop, Eqs. 2-8 with PNQ (Eqs. 44-48), for one query row against one head's keys, float64.
  *   q      : 128 query values (already dequantized)
  *   K, V   : N x 128 key / value values (already dequantized)
  *   Vraw   : N x 128 unquantized values, used on the causal diagonal block
@@ -215,7 +215,7 @@ static void online_softmax_row(const double* q, const double* K, const double* V
   unsigned char* valid = (unsigned char*)malloc(bc);
   for (int64_t j = 0; j < ntiles; j++) {
     const int64_t k0 = j * bc;
-    /* line 11: S = Q^ K^T / sqrt(d) */
+    /* Eq. 2: S = Q^ K^T / sqrt(d) */
     double rowmax = -INFINITY;
     for (int kk = 0; kk < bc; kk++) {
       int64_t key = k0 + kk;
@@ -229,12 +229,12 @@ static void online_softmax_row(const double* q, const double* K, const double* V
       S[kk] = dot * inv_sqrt_d;
       if (S[kk] > rowmax) rowmax = S[kk];
     }
-    /* lines 12-13 */
+    /* Eqs. 3-4: running max and alpha */
     double m_new = m > rowmax ? m : rowmax;
     double alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
-    /* line 14: P~ = exp(S - m_new) */
+    /* Eq. 5: P~ = exp(S - m_new) */
     for (int kk = 0; kk < bc; kk++) Pt[kk] = valid[kk] ? exp(S[kk] - m_new) : 0.0;
-    /* line 15: P^ = Q*(P~), 32-key blocks counted from key 0 */
+    /* Eq. 44: P^ = Q*(P~), 32-key blocks counted from key 0 */
     for (int b0 = 0; b0 < bc; b0 += ORC_BLOCK) {
       if (op->quant_p) {
         uint8_t cb[ORC_BLOCK];
@@ -244,11 +244,11 @@ static void online_softmax_row(const double* q, const double* K, const double* V
         for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = Pt[b0 + t];
       }
     }
-    /* line 16 (PNQ, Eq. 47) or Eq. 16 (direct) */
+    /* Eq. 47 (PNQ) or Eq. 16 (direct placement) */
     double tile_sum = 0.0;
     for (int kk = 0; kk < bc; kk++) tile_sum += (op->placement == 0) ? Ph[kk] : Pt[kk];
     ell = alpha * ell + tile_sum;
-    /* line 17 (Eq. 48): O = diag(alpha) O + P^ V^ */
+    /* Eq. 48: O = diag(alpha) O + P^ V^ */
     for (int c = 0; c < ORC_D; c++) acc[c] *= alpha;
     for (int kk = 0; kk < bc; kk++) {
       if (!valid[kk] || Ph[kk] == 0.0) continue;
@@ -257,11 +257,11 @@ static void online_softmax_row(const double* q, const double* K, const double* V
                                                                                  : V + key * ORC_D;
       for (int c = 0; c < ORC_D; c++) acc[c] += Ph[kk] * vrow[c];
     }
-    m = m_new; /* line 18 */
+    m = m_new;
     if (phat) memcpy(phat + j * bc, Ph, sizeof(double) * bc);
     if (mhist) mhist[j] = m;
   }
-  /* line 20: O = diag(l)^-1 O */
+  /* Eq. 8: O = diag(l)^-1 O */
   for (int c = 0; c < ORC_D; c++) o[c] = acc[c] / ell;
   *ell_out = ell;
   free(S);

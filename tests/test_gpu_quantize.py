@@ -1,7 +1,7 @@
 """GPU parity of the MXFP4 quantizers (C-ABI kernels) against the oracle.
 
 Bit-exact: every E2M1 code and every E8M0 scale byte of Q, K (rotated) and V
-must equal the oracle's ("MXAttention" Algorithm 1 and Algorithm 2 lines 3-7).
+must equal the oracle's ("MXAttention" Algorithm 1 and the quantization steps of Algorithm 2, section 4.3).
 Small workloads are compared in full; the full-size workloads on sampled
 tokens (Q/K) and sampled 128-token windows plus the ragged tail (V), in the
 launch configuration the benchmark times.

@@ -1,5 +1,5 @@
 """Pins of the oracle's fixed Hadamard rotation ("MXAttention" section 4.3,
-Algorithm 2 lines 3-4; explainer page step 1 and glossary).
+Algorithm 2 (section 4.3), rotation step; explainer page step 1 and glossary).
 
 * the rotation matrix recovered from the oracle is +-2^-3.5 times a Sylvester
   Hadamard matrix: H H^T = 128 I exactly (integer check), H[i][j] = (-1)^popcount(i&j)
