@@ -503,51 +503,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence1(lbits);
         float l = __uint_as_float(lbits);
-        const bool diag = kCausal;
-        const float dsc = __uint_as_float(diag_sbyte << 23);  // 2^(byte-127)
-        if (diag) {
+        const float dsc = __uint_as_float(diag_sbyte << 23);  // causal: 2^(byte-127) of the diagonal block
+        if constexpr (kCausal) {
 #pragma unroll
           for (int k = 0; k < 32; k++) l += e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
         }
         const float inv_l = 1.0f / l;
-        // keys of the diagonal block: tile Tg-1, rows 32*quad .. 32*quad+31
-        const int64_t dkey0 = static_cast<int64_t>(Tg - 1) * kTile + 32 * quad;
-        const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_bf16);
+        float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
+        if constexpr (!kCausal) {
 #pragma unroll 1
-        for (int c = 0; c < 4; c++) {
-          uint32_t o[32];
-          tmem_ld32(tl + ocol + 32 * c, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-          float acc[32];
+          for (int c = 0; c < 4; c++) {
+            uint32_t o[32];
+            tmem_ld32(tl + ocol + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+            if (qrow < N) {
+              float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
-          if (diag) {
+              for (int i = 0; i < 8; i++)
+                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                     __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+            }
+          }
+        } else {
+          // The warp's diagonal block is keys 32*quad .. +31 of tile Tg-1 (its own
+          // 32 query rows). Its bf16 V rows pass through shared memory one
+          // 32-channel chunk (2 KB) at a time: lane t loads key t's 64 bytes of
+          // the chunk, the next chunk's loads are in flight while this one is
+          // used, and every thread then reads all 32 rows as broadcasts. The
+          // staging space is this group's two P^ buffers, idle since the o_done
+          // wait above (every P^V^ that read them has completed): 4 KB per warp,
+          // two chunk slots.
+          uint8_t* stage = smem + kOffP + 2 * g * kTileBytes + quad * 4096;
+          const int64_t mykey = static_cast<int64_t>(Tg - 1) * kTile + 32 * quad + lane;
+          const bool key_ok = mykey < N;
+          const uint4* myrow =
+              reinterpret_cast<const uint4*>(p.v_bf16) + (static_cast<int64_t>(bh) * N + (key_ok ? mykey : 0)) * (kD / 8);
+          const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+          uint4 nxt[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; q4++) nxt[q4] = key_ok ? __ldg(myrow + q4) : zero4;
 #pragma unroll 1
-            for (int k = 0; k < 32; k++) {
-              const uint32_t wk = k < 8 ? diag_words[0] : (k < 16 ? diag_words[1] : (k < 24 ? diag_words[2] : diag_words[3]));
-              const float pk = e2m1_decode((wk >> (4 * (k & 7))) & 0xFu) * dsc;
-              const int64_t key = dkey0 + k;
-              if (pk == 0.0f || key >= N) continue;
-              const uint4* row = vsrc + ((static_cast<int64_t>(bh) * N + key) * kD + 32 * c) / 8;
+          for (int c = 0; c < 4; c++) {
+            uint4* slot = reinterpret_cast<uint4*>(stage + (c & 1) * 2048);
 #pragma unroll
-              for (int q4 = 0; q4 < 4; q4++) {
-                const uint4 u = __ldg(row + q4);
-                const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+            for (int q4 = 0; q4 < 4; q4++) slot[lane * 4 + q4] = nxt[q4];
+            if (c < 3) {
 #pragma unroll
-                for (int t2 = 0; t2 < 4; t2++) {
-                  acc[8 * q4 + 2 * t2] = fmaf(pk, __uint_as_float(uu[t2] << 16), acc[8 * q4 + 2 * t2]);
-                  acc[8 * q4 + 2 * t2 + 1] = fmaf(pk, __uint_as_float(uu[t2] & 0xFFFF0000u), acc[8 * q4 + 2 * t2 + 1]);
+              for (int q4 = 0; q4 < 4; q4++) nxt[q4] = key_ok ? __ldg(myrow + 4 * (c + 1) + q4) : zero4;
+            }
+            // slot c&1 was last read in chunk c-2, before every lane passed the
+            // __syncwarp of chunk c-1
+            __syncwarp();
+            uint32_t o[32];
+            tmem_ld32(tl + ocol + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
+            // masked keys (beyond the row or beyond N) have P^ = 0; their staged
+            // rows are finite (zeros past N)
+#pragma unroll 1
+            for (int kk = 0; kk < 4; kk++) {
+              const uint32_t wk = kk == 0 ? diag_words[0] : (kk == 1 ? diag_words[1] : (kk == 2 ? diag_words[2] : diag_words[3]));
+#pragma unroll
+              for (int k = 0; k < 8; k++) {
+                const float pk = e2m1_decode((wk >> (4 * k)) & 0xFu) * dsc;
+                const uint4* vr = slot + (8 * kk + k) * 4;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) {
+                  const uint4 u = vr[q4];
+                  const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int t2 = 0; t2 < 4; t2++) {
+                    acc[8 * q4 + 2 * t2] = fmaf(pk, __uint_as_float(uu[t2] << 16), acc[8 * q4 + 2 * t2]);
+                    acc[8 * q4 + 2 * t2 + 1] = fmaf(pk, __uint_as_float(uu[t2] & 0xFFFF0000u), acc[8 * q4 + 2 * t2 + 1]);
+                  }
                 }
               }
             }
-          }
-          if (qrow < N) {
-            float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + qrow) * kD + 32 * c);
+            if (qrow < N) {
+              float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-              dst[i] = make_float4(acc[4 * i] * inv_l, acc[4 * i + 1] * inv_l, acc[4 * i + 2] * inv_l,
-                                   acc[4 * i + 3] * inv_l);
+              for (int i = 0; i < 8; i++)
+                dst[i] = make_float4(acc[4 * i] * inv_l, acc[4 * i + 1] * inv_l, acc[4 * i + 2] * inv_l,
+                                     acc[4 * i + 3] * inv_l);
+            }
           }
         }
       }
