@@ -87,6 +87,7 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2Qmax = 2.8579809951275723f;  // log2(7.25)
+constexpr float kExpMagic = 12583039.0f;          // 1.5 * 2^23 + 127
 
 struct Params {
   const uint8_t* q_scales;
@@ -374,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty));
 
-      if (j == Tg - 1 && (kCausal || ragged)) {
+      const bool masked = j == Tg - 1 && (kCausal || ragged);
+      if (masked) {
         // keys of this tile visible to the row: i < nvalid (key < N, and key <= row if causal)
         const int64_t key0 = static_cast<int64_t>(j) * kTile;
         int64_t lim = N - key0;
@@ -401,17 +403,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
                           : nullptr;
       const float2 c2 = make_float2(C, C);
-      uint32_t sbytes = 0;
+      // UOS exponents of the four blocks, two at a time on the FMA pipe:
+      // e = ceil(max(bm*C - (m_new*C + log2 7.25), -127)). Adding kExpMagic
+      // (1.5*2^23 + 127) rounding toward +inf lands on kExpMagic + e exactly
+      // (unit spacing there), so the low byte of its bits is the E8M0 byte
+      // e + 127, and kExpMagic - t recovers -e exactly.
+      const float mcq = mc + kLog2Qmax;
+      const float2 xe01 = __ffma2_rn(make_float2(bm[0], bm[1]), c2, make_float2(-mcq, -mcq));
+      const float2 xe23 = __ffma2_rn(make_float2(bm[2], bm[3]), c2, make_float2(-mcq, -mcq));
+      const float2 mg = make_float2(kExpMagic, kExpMagic);
+      const float2 t01 = __fadd2_ru(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
+      const float2 t23 = __fadd2_ru(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
+      // -(mc + e), rounded once as mc + e would be
+      const float2 nmc = make_float2(-mc, -mc), neg1 = make_float2(-1.0f, -1.0f);
+      const float2 no01 = __fadd2_rn(__ffma2_rn(t01, neg1, mg), nmc);
+      const float2 no23 = __fadd2_rn(__ffma2_rn(t23, neg1, mg), nmc);
+      uint32_t sbytes = __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
+                                    __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
+      if (masked) {
+        // all-zero (fully masked) blocks take sigma = 1
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+          if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
+      }
 #pragma unroll
       for (int b = 0; b < 4; b++) {
-        const bool empty = bm[b] == -INFINITY;
-        const float xb = fmaf(bm[b], C, -mc);
-        int e = static_cast<int>(ceilf(xb - kLog2Qmax));
-        e = empty ? -127 : (e < -127 ? -127 : e);
-        const float off = mc + static_cast<float>(e);
-        const uint32_t sbyte = empty ? 127u : static_cast<uint32_t>(e + 127);
-        sbytes |= sbyte << (8 * b);
-        const float2 noff2 = make_float2(-off, -off);
+        const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
+        const float2 noff2 = make_float2(noff, noff);
         uint32_t w[4];
 #pragma unroll
         for (int gq = 0; gq < 4; gq++) {
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             diag_words[gq] = w[gq];
             w[gq] = 0u;
           }
-          diag_sbyte = sbyte;
+          diag_sbyte = (sbytes >> (8 * b)) & 0xFFu;
         }
         *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
