@@ -251,6 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- QK issuer
     if (lane == 0) {
       const uint32_t id0 = idesc_mxf4(128, kTile, 0, 0), id1 = idesc_mxf4(128, kTile, 2, 2);
+      // operand descriptors computed once; a stage or buffer moves only the
+      // start-address field (16-byte units), which cannot carry out of it here
+      const uint64_t dq0 = smem_desc(sb + kOffQ, 16, 512, kSwizzle64B);
+      const uint64_t dk0 = smem_desc(sb + kOffK, 16, 512, kSwizzle64B);
+      const uint64_t dsfk0 = smem_desc(sb + kOffKSF, 0, 128, kSwizzleNone);
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
       if (ok) {
         tc_fence_after();
@@ -263,18 +268,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarKFull + ks), (j / kKStages) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sfk = tmem + kColSFK + 4 * (j & 1);
-        tc_cp_sf(sfk, smem_desc(sb + kOffKSF + ks * kSfAtomBytes, 0, 128, kSwizzleNone));
-        const uint32_t ka = sb + kOffK + ks * kTileBytes;
+        tc_cp_sf(sfk, dsfk0 + ks * (kSfAtomBytes >> 4));
+        const uint64_t dk = dk0 + ks * (kTileBytes >> 4);
         for (int g = 0; g < 2; g++) {
           if (j >= (g ? ntiles1 : ntiles0)) continue;
           // the single S buffer is free once the previous production was read
           if (n >= 1 && !mbar_wait(bar(kBarSEmpty), (n - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t qa = sb + kOffQ + g * kTileBytes, sfq = tmem + kColSFQ + 4 * g;
-          mma_mxf4(tmem + kColS, smem_desc(qa, 16, 512, kSwizzle64B), smem_desc(ka, 16, 512, kSwizzle64B), id0, sfq,
-                   sfk, 0u);
-          mma_mxf4(tmem + kColS, smem_desc(qa + 32, 16, 512, kSwizzle64B), smem_desc(ka + 32, 16, 512, kSwizzle64B),
-                   id1, sfq, sfk, 1u);
+          const uint64_t dq = dq0 + g * (kTileBytes >> 4);
+          const uint32_t sfq = tmem + kColSFQ + 4 * g;
+          mma_mxf4(tmem + kColS, dq, dk, id0, sfq, sfk, 0u);
+          mma_mxf4(tmem + kColS, dq + 2, dk + 2, id1, sfq, sfk, 1u);  // K step 1: +32 bytes
           if (!((p.debug_flags & kDebugNeverArriveS) && n == 0)) tc_commit(bar(kBarSFull + g));
           n++;
         }
@@ -287,6 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- PV issuer
     if (lane == 0) {
       const uint32_t id0 = idesc_mxf4(128, kPvN, 0, 0), id1 = idesc_mxf4(128, kPvN, 2, 2);
+      const uint64_t dp0 = smem_desc(sb + kOffP, 16, 512, kSwizzle64B);
+      const uint64_t dv0 = smem_desc(sb + kOffV, 16, 512, kSwizzle64B);
+      const uint64_t dsfv0 = smem_desc(sb + kOffVSF, 0, 128, kSwizzleNone);
       // scale atom of the ones rows, once into both V scale buffers
       tc_cp_sf(tmem + kColSFV + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
       tc_cp_sf(tmem + kColSFV + 12, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
@@ -294,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < T; j++) {
         const int vs = j % kVStages;
         if (!mbar_wait(bar(kBarVFull + vs), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t va = sb + kOffV + vs * kVTileBytes, sfv = tmem + kColSFV + 8 * (j & 1);
+        const uint64_t dv = dv0 + vs * (kVTileBytes >> 4);
+        const uint32_t sfv = tmem + kColSFV + 8 * (j & 1);
         bool sfv_loaded = false;
         for (int g = 0; g < 2; g++) {
           if (j >= (g ? ntiles1 : ntiles0)) continue;
@@ -303,16 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!sfv_loaded) {
             // the previous user of this buffer (tile j-2) is complete: the softmax
             // threads waited for it before arriving on p_full
-            tc_cp_sf(sfv, smem_desc(sb + kOffVSF + vs * kSfAtomBytes, 0, 128, kSwizzleNone));
+            tc_cp_sf(sfv, dsfv0 + vs * (kSfAtomBytes >> 4));
             sfv_loaded = true;
           }
-          const uint32_t pa = sb + kOffP + (2 * g + (j & 1)) * kTileBytes;
+          const uint64_t dp = dp0 + (2 * g + (j & 1)) * (kTileBytes >> 4);
           const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
           const uint32_t od = tmem + kColO + g * kPvN;
-          mma_mxf4(od, smem_desc(pa, 16, 512, kSwizzle64B), smem_desc(va, 16, 512, kSwizzle64B), id0, sfp, sfv,
-                   j > 0 ? 1u : 0u);
-          mma_mxf4(od, smem_desc(pa + 32, 16, 512, kSwizzle64B), smem_desc(va + 32, 16, 512, kSwizzle64B), id1, sfp,
-                   sfv, 1u);
+          mma_mxf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
+          mma_mxf4(od, dp + 2, dv + 2, id1, sfp, sfv, 1u);
           tc_commit(bar(kBarODone + g));
         }
         if (!ok) break;
