@@ -59,6 +59,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
+        lib.mxattn_quantize_qk_ex.argtypes = [P, I64, I64, I64, I64, I, I, P, P, P]
+        lib.mxattn_quantize_v_ex.argtypes = [P, I64, I64, I64, I64, I, P, P, P]
+        lib.mxattn_forward_ex.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P, P]
         lib.mxattn_attention_host.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, SZ, P]
         lib.mxattn_attention_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_attention_noalloc.restype = I
@@ -69,7 +72,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_set_debug_flags.restype = None
         lib.mxattn_last_error.restype = ctypes.c_char_p
         for name in ("mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward", "mxattn_forward_dump_phat",
-                     "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_check"):
+                     "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_check", "mxattn_quantize_qk_ex",
+                     "mxattn_quantize_v_ex", "mxattn_forward_ex"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -152,6 +156,46 @@ def mxattn_forward_dump_phat(q_codes, q_scales, k_codes, k_scales, v_codes, v_sc
                                            _ptr(v_codes), _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal),
                                            _ptr(out), _ptr(pc), _ptr(ps), _stream(stream)))
     return out, pc, ps
+
+
+# Ablation switches (include/mxattn.h: mxattn_scale_rule, mxattn_placement)
+RULE_UOS, RULE_OCP, RULE_TFS = 0, 1, 2
+PLACE_PNQ, PLACE_DIRECT = 0, 1
+
+
+def mxattn_quantize_qk_ex(x: torch.Tensor, rule: int = RULE_UOS, rotate: bool = True,
+                          codes: torch.Tensor | None = None, scales: torch.Tensor | None = None, stream=None):
+    """Q/K quantization with a chosen scale rule and optional rotation. Returns (codes, scales)."""
+    B, H, N, Dx = _shape(x)
+    nc, ns = qk_layout_sizes(B, H, N)
+    codes = torch.empty(nc, dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = torch.empty(ns, dtype=torch.uint8, device=x.device) if scales is None else scales
+    _raise(load().mxattn_quantize_qk_ex(_ptr(x), B, H, N, Dx, int(rule), int(bool(rotate)), _ptr(codes),
+                                        _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def mxattn_quantize_v_ex(v: torch.Tensor, rule: int = RULE_UOS, codes: torch.Tensor | None = None,
+                         scales: torch.Tensor | None = None, stream=None):
+    """V quantization with a chosen scale rule. Returns (codes, scales)."""
+    B, H, N, Dx = _shape(v)
+    nc, ns = v_layout_sizes(B, H, N)
+    codes = torch.empty(nc, dtype=torch.uint8, device=v.device) if codes is None else codes
+    scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
+    _raise(load().mxattn_quantize_v_ex(_ptr(v), B, H, N, Dx, int(rule), _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def mxattn_forward_ex(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
+                      causal: bool = False, p_rule: int = RULE_UOS, placement: int = PLACE_PNQ,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Forward with the P~ scale rule and the l placement as switches. Returns fp32 [B, H, N, 128]."""
+    dev = q_codes.device
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
+    _raise(load().mxattn_forward_ex(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+                                    _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), int(p_rule),
+                                    int(placement), _ptr(out), _stream(stream)))
+    return out
 
 
 def mxattn_forward_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,

@@ -87,6 +87,7 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2Qmax = 2.8579809951275723f;  // log2(7.25)
+constexpr float kLog2Six = 2.5849625007211563f;   // log2(6): TFS scale
 constexpr float kExpMagic = 12583039.0f;          // 1.5 * 2^23 + 127
 
 struct Params {
@@ -102,6 +103,8 @@ struct Params {
   int NT;
   int causal;
   uint32_t debug_flags;
+  int p_rule;     // variant kernels only
+  int placement;  // variant kernels only
   float score_scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -134,8 +137,11 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
 }
 
 // kCausal and kDump are compile-time so the non-causal, non-diagnostic path
-// carries no checks for either.
-template <bool kCausal, bool kDump>
+// carries no checks for either. kVariant builds the ablation variants of
+// section 5.4 (Table 3): the P~ blocks take the scale rule p.p_rule (UOS, OCP
+// floor of Eq. 11, TFS of Eq. 14) and l may come from the unquantized P~
+// (direct placement, Eqs. 16-17) instead of P^ (PNQ, Eq. 47).
+template <bool kCausal, bool kDump, bool kVariant>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -342,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool my_abort = false;
     uint32_t diag_words[4] = {0u, 0u, 0u, 0u};  // causal: P^ codes of the query's own 32-key block
     uint32_t diag_sbyte = 127;
+    float l_direct = 0.0f;  // variant kernels, direct placement: l from P~ (Eq. 16)
     // all lanes poll; the outcome is made warp-uniform so tcgen05 .sync.aligned ops stay convergent
     auto wait_uniform = [&](int b, uint32_t parity) {
       bool ok = !my_abort && mbar_wait(bar(b), parity, abort_flag);
@@ -410,16 +417,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : nullptr;
       const float2 c2 = make_float2(C, C);
       // UOS exponents of the four blocks, two at a time on the FMA pipe:
-      // e = ceil(max(bm*C - (m_new*C + log2 7.25), -127)). Adding kExpMagic
+      // e = ceil(max((bm - m_new)*C - log2 7.25, -127)). The block's offset
+      // bm - m_new is formed first, so the block holding the row maximum has
+      // log2 of its P~ maximum exactly 0 (this matters where a rule's
+      // boundary lies on an integer, as for the OCP floor). Adding kExpMagic
       // (1.5*2^23 + 127) rounding toward +inf lands on kExpMagic + e exactly
       // (unit spacing there), so the low byte of its bits is the E8M0 byte
       // e + 127, and kExpMagic - t recovers -e exactly.
-      const float mcq = mc + kLog2Qmax;
-      const float2 xe01 = __ffma2_rn(make_float2(bm[0], bm[1]), c2, make_float2(-mcq, -mcq));
-      const float2 xe23 = __ffma2_rn(make_float2(bm[2], bm[3]), c2, make_float2(-mcq, -mcq));
+      float qoff = kLog2Qmax;
+      if constexpr (kVariant) qoff = p.p_rule == kRuleTFS ? kLog2Six : (p.p_rule == kRuleOCP ? 2.0f : kLog2Qmax);
+      const float2 nm2 = make_float2(-m_new, -m_new), nq2 = make_float2(-qoff, -qoff);
+      const float2 xe01 = __ffma2_rn(__fadd2_rn(make_float2(bm[0], bm[1]), nm2), c2, nq2);
+      const float2 xe23 = __ffma2_rn(__fadd2_rn(make_float2(bm[2], bm[3]), nm2), c2, nq2);
       const float2 mg = make_float2(kExpMagic, kExpMagic);
-      const float2 t01 = __fadd2_ru(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
-      const float2 t23 = __fadd2_ru(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
+      float2 t01, t23;
+      if (kVariant && p.p_rule == kRuleOCP) {
+        // OCP: e = floor(log2 M) - 2, the same add rounding toward -inf
+        t01 = __fadd2_rd(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
+        t23 = __fadd2_rd(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
+      } else {
+        t01 = __fadd2_ru(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
+        t23 = __fadd2_ru(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
+      }
       // -(mc + e), rounded once as mc + e would be
       const float2 nmc = make_float2(-mc, -mc), neg1 = make_float2(-1.0f, -1.0f);
       const float2 no01 = __fadd2_rn(__ffma2_rn(t01, neg1, mg), nmc);
@@ -432,11 +451,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 4; b++)
           if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
       }
+      float tile_ptilde = 0.0f;  // direct placement: sum of this row's P~ over the tile
 #pragma unroll
       for (int b = 0; b < 4; b++) {
         const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
         const float2 noff2 = make_float2(noff, noff);
         uint32_t w[4];
+        float2 ysum = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int gq = 0; gq < 4; gq++) {
           float y[8];
@@ -445,8 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
             y[i] = ex2_approx(x.x);
             y[i + 1] = ex2_approx(x.y);
+            if constexpr (kVariant) ysum = __fadd2_rn(ysum, make_float2(y[i], y[i + 1]));
           }
           w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+        }
+        if constexpr (kVariant) {
+          // y = P~ / 2^e of the block; 2^e from the scale byte (byte 0 is 2^-127)
+          const uint32_t sb_b = (sbytes >> (8 * b)) & 0xFFu;
+          const float scale = sb_b ? __uint_as_float(sb_b << 23) : __uint_as_float(0x00400000u);
+          tile_ptilde = fmaf(ysum.x + ysum.y, scale, tile_ptilde);
         }
         if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
         if (diag_tile && b == quad) {
@@ -467,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
       fence_proxy_async_smem();
       tmem_wait_st();
+      if constexpr (kVariant) l_direct = fmaf(ex2_approx((m_run - m_new) * C), l_direct, tile_ptilde);
       if (j >= 1) {
         // O_g is stable once P^V^ of tile j-1 completes; rescale by alpha if any row's max moved
         const float alpha = ex2_approx((m_run - m_new) * C);
@@ -528,10 +557,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence1(lbits);
         float l = __uint_as_float(lbits);
         const float dsc = __uint_as_float(diag_sbyte << 23);  // causal: 2^(byte-127) of the diagonal block
+        const bool direct = kVariant && p.placement == kPlaceDirect;
         if constexpr (kCausal) {
+          // the diagonal block's P^ is not in the tensor-core sum; direct
+          // placement already counted its P~
+          if (!direct) {
 #pragma unroll
-          for (int k = 0; k < 32; k++) l += e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
+            for (int k = 0; k < 32; k++) l += e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
+          }
         }
+        if (direct) l = l_direct;
         const float inv_l = 1.0f / l;
         float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
         if constexpr (!kCausal) {
@@ -661,6 +696,8 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.NT = static_cast<int>(NT);
   p.causal = a.causal;
   p.debug_flags = a.debug_flags;
+  p.p_rule = a.p_rule;
+  p.placement = a.placement;
   p.score_scale_log2 = kLog2e / 11.313708498984761f;  // log2(e) / sqrt(128)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -668,8 +705,9 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   static bool attr_set[64] = {false};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    for (auto fn : {mxfp4_fwd_kernel<false, false>, mxfp4_fwd_kernel<true, false>, mxfp4_fwd_kernel<false, true>,
-                    mxfp4_fwd_kernel<true, true>}) {
+    for (auto fn : {mxfp4_fwd_kernel<false, false, false>, mxfp4_fwd_kernel<true, false, false>,
+                    mxfp4_fwd_kernel<false, true, false>, mxfp4_fwd_kernel<true, true, false>,
+                    mxfp4_fwd_kernel<false, false, true>, mxfp4_fwd_kernel<true, false, true>}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
     }
@@ -677,12 +715,17 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   }
   dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
   const bool dump = a.phat_codes != nullptr;
-  if (a.causal) {
-    if (dump) mxfp4_fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ;
+  if (variant && dump) return cudaErrorNotSupported;  // the P^ dump covers UOS + PNQ only
+  if (variant) {
+    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  } else if (a.causal) {
+    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   } else {
-    if (dump) mxfp4_fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
 }

@@ -5,7 +5,9 @@
 //  (a) rotate_quantize_qk: per token, Hadamard-rotate the 128 channels
 //      (binary32 butterflies h = 1,2,...,64, then x 2^-3.5 rounded to binary32)
 //      and quantize each 32-channel block to E2M1 with the UOS scale
-//      e = ceil(log2(M / 7.25)).
+//      e = ceil(log2(M / 7.25)). The ablation variants (section 5.4, Table 3)
+//      skip the rotation and/or use the OCP scale e = floor(log2 M) - 2
+//      (Eq. 11) or the TFS scale e = ceil(log2(M / 6)) (Eq. 14).
 //  (b) quantize_v: per channel, quantize blocks of 32 consecutive tokens
 //      (blocks counted from token 0, last block zero-padded) and store the codes
 //      transposed (token-contiguous), the K-major layout the P.V MMA reads.
@@ -28,15 +30,23 @@ namespace {
 
 constexpr float kRotScale = 0x1.6a09e6p-4f;  // binary32 nearest to 2^-3.5 = 1/sqrt(128)
 
-// UOS exponent for a finite block maximum M > 0:
-// M = 1.f * 2^(b-127) => ceil(log2(M/7.25)) = (b-126) - 3 if 1.f <= 1.8125 else (b-126) - 2.
-// Denormal maxima and anything below the E8M0 range clamp to -127.
-__device__ __forceinline__ int uos_exponent(float M) {
+// Block scale exponent for a finite block maximum M > 0, M = 1.f * 2^(b-127):
+//   UOS  ceil(log2(M/7.25)) = (b-126) - 3 if 1.f <= 1.8125 else (b-126) - 2
+//   TFS  ceil(log2(M/6))    = (b-126) - 3 if 1.f <= 1.5    else (b-126) - 2
+//   OCP  floor(log2 M) - 2  = (b-126) - 3
+// i.e. one comparison of the mantissa field against mant_thr (0x680000,
+// 0x400000, or 0x7FFFFF so that it always holds). Denormal maxima and
+// anything below the E8M0 range clamp to -127.
+__device__ __forceinline__ int block_exponent(float M, uint32_t mant_thr) {
   const uint32_t bits = __float_as_uint(M);
   const int b = static_cast<int>(bits >> 23);
   if (b == 0) return -127;
-  const int e = b - 126 - ((bits & 0x7FFFFFu) <= 0x680000u ? 3 : 2);
+  const int e = b - 126 - ((bits & 0x7FFFFFu) <= mant_thr ? 3 : 2);
   return e < -127 ? -127 : e;
+}
+
+uint32_t rule_mantissa_threshold(int rule) {
+  return rule == kRuleOCP ? 0x7FFFFFu : (rule == kRuleTFS ? 0x400000u : 0x680000u);
 }
 
 // 2^-e as binary32; valid for e in [-127, 126], which covers every finite M.
@@ -63,7 +73,8 @@ constexpr int kQkThreads = 256;
 __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const uint4* __restrict__ x,
                                                                          uint32_t* __restrict__ codes,
                                                                          uint32_t* __restrict__ scales,
-                                                                         int64_t BH, int64_t N, int64_t NT) {
+                                                                         int64_t BH, int64_t N, int64_t NT,
+                                                                         uint32_t mant_thr, int rotate) {
   const int lane = threadIdx.x & 31;
   const int l = lane & 15;
   const int64_t slots_per_head = NT * kTile;
@@ -87,6 +98,7 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
 #pragma unroll
       for (int i = 0; i < 8; i++) z[i] = 0.0f;
     }
+    if (rotate) {
     // in-lane butterflies: h = 1, 2, 4
 #pragma unroll
     for (int h = 1; h < 8; h <<= 1) {
@@ -108,19 +120,19 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
         z[i] = upper ? __fsub_rn(p, z[i]) : __fadd_rn(z[i], p);
       }
     }
+#pragma unroll
+    for (int i = 0; i < 8; i++) z[i] = __fmul_rn(z[i], kRotScale);
+    }
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      z[i] = __fmul_rn(z[i], kRotScale);
-      m = fmaxf(m, fabsf(z[i]));
-    }
+    for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(z[i]));
     // block = 32 channels = lanes 4b..4b+3 of the token
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     uint32_t word = 0;
     uint32_t sbyte = 127;
     if (m > 0.0f) {
-      const int e = uos_exponent(m);
+      const int e = block_exponent(m, mant_thr);
       const float inv = pow2_neg(e);
       word = pack_e2m1x8(__fmul_rn(z[0], inv), __fmul_rn(z[1], inv), __fmul_rn(z[2], inv),
                          __fmul_rn(z[3], inv), __fmul_rn(z[4], inv), __fmul_rn(z[5], inv),
@@ -147,7 +159,7 @@ constexpr int kVRowWords = kD / 2 + 1;  // bf16x2 words per staged token row (+1
 __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __restrict__ v,
                                                                 uint8_t* __restrict__ codes,
                                                                 uint32_t* __restrict__ scales, int64_t N,
-                                                                int64_t NT, int64_t row_bytes) {
+                                                                int64_t NT, int64_t row_bytes, uint32_t mant_thr) {
   __shared__ uint32_t tile[kTile * kVRowWords];
   const int64_t t = blockIdx.x;
   const int64_t bh = blockIdx.y;
@@ -183,7 +195,7 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
     uint32_t sbyte = 127;
     uint4 packed = make_uint4(0, 0, 0, 0);
     if (m > 0.0f) {
-      const int e = uos_exponent(m);
+      const int e = block_exponent(m, mant_thr);
       const float inv = pow2_neg(e);
       uint32_t w4[4];
 #pragma unroll
@@ -207,8 +219,8 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
 
 }  // namespace
 
-cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales,
-                                      cudaStream_t s) {
+cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
+                                      int rotate, cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);
   const int64_t pairs = ceil_div(BH * NT * kTile, 2);
   int dev = 0, sms = 0;
@@ -218,17 +230,19 @@ cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void
   const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
   rotate_quantize_qk_kernel<<<grid, kQkThreads, 0, s>>>(static_cast<const uint4*>(x),
                                                         static_cast<uint32_t*>(codes),
-                                                        static_cast<uint32_t*>(scales), BH, N, NT);
+                                                        static_cast<uint32_t*>(scales), BH, N, NT,
+                                                        rule_mantissa_threshold(rule), rotate);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales,
+cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                               cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);
   const int64_t row_bytes = ceil_div(N, kBlock) * kBlock / 2;
   dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
   quantize_v_kernel<<<grid, kVThreads, 0, s>>>(static_cast<const uint4*>(v), static_cast<uint8_t*>(codes),
-                                               static_cast<uint32_t*>(scales), N, NT, row_bytes);
+                                               static_cast<uint32_t*>(scales), N, NT, row_bytes,
+                                               rule_mantissa_threshold(rule));
   return cudaGetLastError();
 }
 

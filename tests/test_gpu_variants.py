@@ -1,0 +1,136 @@
+"""GPU parity of the ablation variants ("MXAttention" section 5.4, Table 3)
+against the oracle, through the C ABI.
+
+Switches: the block scale rule of every quantizer (UOS, Eq. 13; OCP floor,
+Eq. 11; TFS ceil, Eq. 14), the fixed Hadamard rotation on or off, and where
+l comes from (PNQ, Eq. 47, or direct placement, Eqs. 16-17).
+  * quantizers: every code and scale byte equals the oracle's;
+  * forward: max |O_gpu - O_oracle| <= 2e-3 * RMS(O_oracle) on every row of
+    small cases (ragged N, causal and not), for the rows of Table 3 and TFS;
+  * row-sum control (Proposition 1 vs Eq. 110): with V == 1, PNQ gives
+    O == 1 while direct placement gives rows that are not 1, as the oracle
+    does.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import _layouts as L
+from mxfp4_precision_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL_RMS = 2e-3
+
+# (name, rule of Q/K/V/P~, rotate, placement) -- Table 3 top to bottom, then TFS
+CONFIGS = [
+    ("full", 0, True, 0),
+    ("no_uos", 1, True, 0),
+    ("no_uos_no_pnq", 1, True, 1),
+    ("ocp_direct", 1, False, 1),
+    ("tfs_pnq", 2, True, 0),
+]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mxfp4_precision_attention_gb300 as m
+
+    m.load()
+    return m
+
+
+@pytest.mark.parametrize("rule", [0, 1, 2])
+@pytest.mark.parametrize("rotate", [True, False])
+def test_quantize_qk_rules(mx, orc, rule, rotate):
+    q, _, _ = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", H=3, N=1000)
+    B, H, N, _ = q.shape
+    codes, scales = mx.mxattn_quantize_qk_ex(q, rule=rule, rotate=rotate)
+    torch.cuda.synchronize()
+    gc = L.qk_codes_logical(codes.cpu().numpy(), B * H, N)
+    gs_all = L.tiles_logical(scales.cpu().numpy(), B * H, N)
+    assert np.all(gs_all[:, N:] == 127)
+    oc, os_ = orc.rotate_quantize_qk(W.as_u16(q).reshape(B * H, N, 128), rule=rule, rotate=rotate)
+    assert np.array_equal(gc, oc), f"code mismatches: {(gc != oc).sum()}"
+    assert np.array_equal(gs_all[:, :N], os_), f"scale mismatches: {(gs_all[:, :N] != os_).sum()}"
+
+
+@pytest.mark.parametrize("rule", [0, 1, 2])
+def test_quantize_v_rules(mx, orc, rule):
+    _, _, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", H=3, N=1000)
+    B, H, N, _ = v.shape
+    codes, scales = mx.mxattn_quantize_v_ex(v, rule=rule)
+    torch.cuda.synchronize()
+    gc = L.v_codes_logical(codes.cpu().numpy(), B * H, N)
+    gs = L.v_scales_logical(scales.cpu().numpy(), B * H, N)
+    oc, os_ = orc.quantize_v(W.as_u16(v).reshape(B * H, N, 128), rule=rule)
+    assert np.array_equal(gc, oc), f"code mismatches: {(gc != oc).sum()}"
+    assert np.array_equal(gs, os_), f"scale mismatches: {(gs != os_).sum()}"
+
+
+def _run_gpu(mx, q, k, v, rule, rotate, placement, causal):
+    B, H, N, _ = q.shape
+    qc, qs = mx.mxattn_quantize_qk_ex(q, rule=rule, rotate=rotate)
+    kc, ks = mx.mxattn_quantize_qk_ex(k, rule=rule, rotate=rotate)
+    vc, vs = mx.mxattn_quantize_v_ex(v, rule=rule)
+    out = mx.mxattn_forward_ex(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal, p_rule=rule, placement=placement)
+    mx.mxattn_check()
+    return out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
+
+
+def _run_oracle(orc, q, k, v, rule, rotate, placement, causal):
+    B, H, N, _ = q.shape
+    qb, kb, vb = (W.as_u16(t).reshape(B * H, N, 128) for t in (q, k, v))
+    qc, qs = orc.rotate_quantize_qk(qb, rule=rule, rotate=rotate)
+    kc, ks = orc.rotate_quantize_qk(kb, rule=rule, rotate=rotate)
+    vc, vs = orc.quantize_v(vb, rule=rule)
+    rows = np.array([[b, i] for b in range(B * H) for i in range(N)], dtype=np.int64)
+    ref = orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=vb, causal=causal, placement=placement, p_rule=rule)
+    return ref["out"].reshape(B * H, N, 128)
+
+
+@pytest.mark.parametrize("name,rule,rotate,placement", CONFIGS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_variants_all_rows(mx, orc, name, rule, rotate, placement, causal):
+    if causal:
+        q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=700, seed=13)
+    else:
+        q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=300)
+    g = _run_gpu(mx, q, k, v, rule, rotate, placement, causal)
+    o = _run_oracle(orc, q, k, v, rule, rotate, placement, causal)
+    err = np.abs(g - o).max()
+    rms = math.sqrt(np.mean(o ** 2))
+    print(f"{name} causal={causal}: max|err| = {err:.3e}, RMS = {rms:.3e}, ratio = {err / rms:.3e}")
+    assert err <= TOL_REL_RMS * rms
+
+
+def test_default_switches_equal_plain_entry_points(mx):
+    """UOS + rotation + PNQ through the variant calls is the plain path, bit for bit."""
+    q, k, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", H=2, N=1000)
+    B, H, N, _ = q.shape
+    a = _run_gpu(mx, q, k, v, 0, True, 0, False)
+    qc, qs = mx.mxattn_rotate_quantize_qk(q)
+    kc, ks = mx.mxattn_rotate_quantize_qk(k)
+    vc, vs = mx.mxattn_quantize_v(v)
+    b = mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N).reshape(B * H, N, 128).cpu().numpy()
+    assert np.array_equal(a, b.astype(np.float64))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rowsum_control_v_ones(mx, orc, causal):
+    """V == 1: PNQ rows are exactly normalized (Proposition 1); direct placement rows
+    are not (Eq. 110), on the GPU and on the oracle alike."""
+    q, k, _ = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=600, seed=21)
+    v = torch.ones_like(q)
+    pnq = _run_gpu(mx, q, k, v, 0, True, 0, causal)
+    direct = _run_gpu(mx, q, k, v, 0, True, 1, causal)
+    assert np.abs(pnq - 1.0).max() <= 1e-5
+    dev_gpu = np.abs(direct - 1.0).max()
+    dev_ora = np.abs(_run_oracle(orc, q, k, v, 0, True, 1, causal) - 1.0).max()
+    print(f"direct placement, V == 1: max |O - 1| gpu {dev_gpu:.3e}, oracle {dev_ora:.3e}")
+    assert dev_gpu > 1e-3 and dev_ora > 1e-3
+
