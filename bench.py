@@ -355,6 +355,81 @@ def run_ours(args, w):
         torch.distributed.destroy_process_group()
 
 
+# Table 3 of the paper (section 5.4), top to bottom, then TFS:
+# (name, scale rule of Q/K/V/P~, rotate, placement of l)
+ABLATION = [
+    ("full (rotation + PNQ + UOS)", 0, True, 0),
+    ("without UOS (OCP)", 1, True, 0),
+    ("without UOS, PNQ (OCP + direct l)", 1, True, 1),
+    ("plain OCP MXFP4 (no rotation, direct l)", 1, False, 1),
+    ("rotation + PNQ + TFS", 2, True, 0),
+]
+
+
+def run_accuracy(args):
+    """Accuracy of the ablation variants and the BF16 path against exact
+    softmax attention (Eq. 1, float64 on the host) on sampled rows of every
+    workload, plus the mean row sum of the normalized attention under direct
+    placement (V = 1 makes the output the row sum). Prints one JSON line."""
+    import torch
+
+    import mxfp4_precision_attention_gb300 as mx
+    from mxfp4_precision_attention_gb300 import workloads as W
+
+    mx.load()
+    names = args.accuracy_workloads.split(",") if args.accuracy_workloads else list(W.WORKLOADS)
+    table = {}
+    for wname in names:
+        w = W.WORKLOADS[wname]
+        q, k, v = W.generate(w, device="cuda")
+        B, H, N = w.B, w.H, w.N
+        g = torch.Generator().manual_seed(1234)
+        heads = torch.randperm(B * H, generator=g)[: min(4, B * H)].tolist()
+        per_head = max(1, args.accuracy_rows // len(heads))
+        rows = [(h, int(i)) for h in heads for i in torch.randint(0, N, (per_head,), generator=g)]
+        qf, kf, vf = (t.reshape(B * H, N, 128) for t in (q, k, v))
+        ref = []
+        for h, i in rows:  # exact attention for the sampled rows (float64, host)
+            kk = kf[h].double().cpu()
+            s = (qf[h, i].double().cpu() @ kk.T) / 128 ** 0.5
+            if w.causal:
+                s[i + 1:] = -float("inf")
+            ref.append(torch.softmax(s, 0) @ vf[h].double().cpu())
+        ref = torch.stack(ref)
+        hh = torch.tensor([r[0] for r in rows])
+        ii = torch.tensor([r[1] for r in rows])
+
+        def score(out):
+            o = out.reshape(B * H, N, 128)[hh.to(out.device), ii.to(out.device)].double().cpu()
+            cos = torch.nn.functional.cosine_similarity(o, ref, dim=1).mean().item()
+            rel = ((o - ref).norm() / ref.norm()).item()
+            return {"cosine": cos, "rel_l2": rel, "max_abs": (o - ref).abs().max().item()}
+
+        res = {}
+        for name, rule, rotate, placement in ABLATION:
+            qc, qs = mx.mxattn_quantize_qk_ex(q, rule=rule, rotate=rotate)
+            kc, ks = mx.mxattn_quantize_qk_ex(k, rule=rule, rotate=rotate)
+            vc, vs = mx.mxattn_quantize_v_ex(v, rule=rule)
+            out = mx.mxattn_forward_ex(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=w.causal, p_rule=rule,
+                                       placement=placement)
+            mx.mxattn_check()
+            res[name] = score(out)
+            if placement == 1:
+                ones = torch.ones_like(v)
+                oc, os_ = mx.mxattn_quantize_v_ex(ones, rule=rule)
+                rs = mx.mxattn_forward_ex(qc, qs, kc, ks, oc, os_, ones, B, H, N, causal=w.causal, p_rule=rule,
+                                          placement=placement)[..., 0]
+                res[name]["rowsum_mean"] = rs.mean().item()
+                res[name]["rowsum_min"] = rs.min().item()
+        res["bf16 path"] = score(mx.mxattn_forward_bf16(q, k, v, causal=w.causal))
+        mx.mxattn_check()
+        table[wname] = {"rows": len(rows), "results": res}
+        del q, k, v
+        torch.cuda.empty_cache()
+    print(json.dumps({"accuracy": table, "reference": "exact softmax attention (Eq. 1), float64 on the host",
+                      "data": "synthetic"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,7 +443,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
+    ap.add_argument("--accuracy", action="store_true",
+                    help="accuracy of the ablation variants vs exact attention instead of timing")
+    ap.add_argument("--accuracy-workloads", default=None, help="comma-separated workload names (default: all)")
+    ap.add_argument("--accuracy-rows", type=int, default=256, help="sampled query rows per workload")
     args = ap.parse_args()
+    if args.accuracy:
+        run_accuracy(args)
+        return
     from mxfp4_precision_attention_gb300 import workloads as W
 
     w = W.WORKLOADS[args.workload]
