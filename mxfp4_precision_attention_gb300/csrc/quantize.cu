@@ -66,9 +66,31 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
 }
 
 // ----------------------------------------------------------------- (a)
-// 16 lanes per token, 8 consecutive channels per lane (channel 8*l + i).
-// Butterflies h = 1, 2, 4 are in-lane; h = 8..64 pair lanes l and l^(h/8).
+// Four lanes per token. Lane l holds the 8-channel chunks c = 4k + l
+// (k = 0..3), i.e. z[8k + i] is channel 8(4k + l) + i. In this layout the
+// butterflies h = 1, 2, 4 (inside a chunk) and h = 32, 64 (chunk k ^ 1,
+// k ^ 2) stay in the lane; only h = 8 and h = 16 pair lanes l ^ 1 and l ^ 2.
+// Each load instruction reads whole 64-byte segments of 8 token rows.
 constexpr int kQkThreads = 256;
+constexpr int kQkLanesPerToken = 4;
+
+// One butterfly on a register pair: (a, b) -> (a + b, a - b) in binary32.
+__device__ __forceinline__ void bfly(float& a, float& b) {
+  const float s = __fadd_rn(a, b), d = __fsub_rn(a, b);
+  a = s;
+  b = d;
+}
+// Two butterflies at once: (a0,a1), (b0,b1) -> (a + b, a - b) per component.
+// a - b is formed as fma(b, -1, a): the product is exact, so it rounds once,
+// exactly like a subtraction.
+__device__ __forceinline__ void bfly2(float& a0, float& a1, float& b0, float& b1) {
+  const float2 a = make_float2(a0, a1), b = make_float2(b0, b1);
+  const float2 s = __fadd2_rn(a, b), d = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+  a0 = s.x;
+  a1 = s.y;
+  b0 = d.x;
+  b1 = d.y;
+}
 
 __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const uint4* __restrict__ x,
                                                                          uint32_t* __restrict__ codes,
@@ -76,73 +98,106 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
                                                                          int64_t BH, int64_t N, int64_t NT,
                                                                          uint32_t mant_thr, int rotate) {
   const int lane = threadIdx.x & 31;
-  const int l = lane & 15;
+  const int l = lane & 3;
   const int64_t slots_per_head = NT * kTile;
   const int64_t total_slots = BH * slots_per_head;
+  constexpr int kTokPerWarp = 32 / kQkLanesPerToken;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kQkThreads / 32);
-  for (int64_t pair = static_cast<int64_t>(blockIdx.x) * (kQkThreads / 32) + threadIdx.x / 32;
-       pair * 2 < total_slots; pair += warps_total) {
-    const int64_t slot = pair * 2 + (lane >> 4);
+  // h = 8, 16: the lane holding the lower channel of the pair adds, the other subtracts
+  const float sgn8 = (l & 1) ? -1.0f : 1.0f, sgn16 = (l & 2) ? -1.0f : 1.0f;
+  for (int64_t grp = static_cast<int64_t>(blockIdx.x) * (kQkThreads / 32) + threadIdx.x / 32;
+       grp * kTokPerWarp < total_slots; grp += warps_total) {
+    const int64_t slot = grp * kTokPerWarp + lane / kQkLanesPerToken;
     const bool in_range = slot < total_slots;
     const int64_t bh = in_range ? slot / slots_per_head : 0;
     const int64_t n = in_range ? slot - bh * slots_per_head : 0;
     const bool real = in_range && n < N;
-    float z[8];
+    float z[32];
     if (real) {
-      const uint4 raw = ld_nc_v4(x + (bh * N + n) * 16 + l);
-      bf16x2_to_f32(raw.x, z[0], z[1]);
-      bf16x2_to_f32(raw.y, z[2], z[3]);
-      bf16x2_to_f32(raw.z, z[4], z[5]);
-      bf16x2_to_f32(raw.w, z[6], z[7]);
+      const uint4* row = x + (bh * N + n) * 16;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint4 raw = ld_nc_v4(row + 4 * k + l);
+        bf16x2_to_f32(raw.x, z[8 * k + 0], z[8 * k + 1]);
+        bf16x2_to_f32(raw.y, z[8 * k + 2], z[8 * k + 3]);
+        bf16x2_to_f32(raw.z, z[8 * k + 4], z[8 * k + 5]);
+        bf16x2_to_f32(raw.w, z[8 * k + 6], z[8 * k + 7]);
+      }
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; i++) z[i] = 0.0f;
+      for (int i = 0; i < 32; i++) z[i] = 0.0f;
     }
     if (rotate) {
-    // in-lane butterflies: h = 1, 2, 4
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
+      for (int k = 0; k < 4; k++) {
+        float* c = z + 8 * k;
+        // h = 1
+        bfly(c[0], c[1]);
+        bfly(c[2], c[3]);
+        bfly(c[4], c[5]);
+        bfly(c[6], c[7]);
+        // h = 2
+        bfly2(c[0], c[1], c[2], c[3]);
+        bfly2(c[4], c[5], c[6], c[7]);
+        // h = 4
+        bfly2(c[0], c[1], c[4], c[5]);
+        bfly2(c[2], c[3], c[6], c[7]);
+      }
+      // h = 8 (lane ^ 1), h = 16 (lane ^ 2): new = own * sign + partner
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        if (i & h) continue;
-        const float a = z[i], b = z[i + h];
-        z[i] = __fadd_rn(a, b);
-        z[i + h] = __fsub_rn(a, b);
+      for (int st = 0; st < 2; st++) {
+        const int mask = st ? 2 : 1;
+        const float sg = st ? sgn16 : sgn8;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = __shfl_xor_sync(0xffffffffu, z[i], mask);
+          const float p1 = __shfl_xor_sync(0xffffffffu, z[i + 1], mask);
+          const float2 r = __ffma2_rn(make_float2(z[i], z[i + 1]), make_float2(sg, sg), make_float2(p0, p1));
+          z[i] = r.x;
+          z[i + 1] = r.y;
+        }
+      }
+      // h = 32 (chunk k ^ 1), h = 64 (chunk k ^ 2)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        bfly2(z[i], z[i + 1], z[8 + i], z[9 + i]);
+        bfly2(z[16 + i], z[17 + i], z[24 + i], z[25 + i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        bfly2(z[i], z[i + 1], z[16 + i], z[17 + i]);
+        bfly2(z[8 + i], z[9 + i], z[24 + i], z[25 + i]);
+      }
+      const float2 rs = make_float2(kRotScale, kRotScale);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 r = __fmul2_rn(make_float2(z[i], z[i + 1]), rs);
+        z[i] = r.x;
+        z[i + 1] = r.y;
       }
     }
-    // cross-lane butterflies: h = 8, 16, 32, 64 <-> lane xor 1, 2, 4, 8
+    // block k = channels 32k .. 32k+31 = chunk k of the token's four lanes
+    uint32_t sw = 0;
 #pragma unroll
-    for (int s = 1; s < 16; s <<= 1) {
-      const bool upper = (l & s) != 0;
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const float p = __shfl_xor_sync(0xffffffffu, z[i], s);
-        z[i] = upper ? __fsub_rn(p, z[i]) : __fadd_rn(z[i], p);
+    for (int k = 0; k < 4; k++) {
+      const float* c = z + 8 * k;
+      float m = fmaxf(fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3]))),
+                      fmaxf(fmaxf(fabsf(c[4]), fabsf(c[5])), fmaxf(fabsf(c[6]), fabsf(c[7]))));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      uint32_t word = 0;
+      uint32_t sbyte = 127;
+      if (m > 0.0f) {
+        const int e = block_exponent(m, mant_thr);
+        const float2 inv = make_float2(pow2_neg(e), pow2_neg(e));
+        const float2 a = __fmul2_rn(make_float2(c[0], c[1]), inv), b = __fmul2_rn(make_float2(c[2], c[3]), inv);
+        const float2 cc = __fmul2_rn(make_float2(c[4], c[5]), inv), d = __fmul2_rn(make_float2(c[6], c[7]), inv);
+        word = pack_e2m1x8(a.x, a.y, b.x, b.y, cc.x, cc.y, d.x, d.y);
+        sbyte = static_cast<uint32_t>(e + 127);
       }
+      if (real) codes[(bh * N + n) * 16 + 4 * k + l] = word;
+      sw |= sbyte << (8 * k);
     }
-#pragma unroll
-    for (int i = 0; i < 8; i++) z[i] = __fmul_rn(z[i], kRotScale);
-    }
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(z[i]));
-    // block = 32 channels = lanes 4b..4b+3 of the token
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    uint32_t word = 0;
-    uint32_t sbyte = 127;
-    if (m > 0.0f) {
-      const int e = block_exponent(m, mant_thr);
-      const float inv = pow2_neg(e);
-      word = pack_e2m1x8(__fmul_rn(z[0], inv), __fmul_rn(z[1], inv), __fmul_rn(z[2], inv),
-                         __fmul_rn(z[3], inv), __fmul_rn(z[4], inv), __fmul_rn(z[5], inv),
-                         __fmul_rn(z[6], inv), __fmul_rn(z[7], inv));
-      sbyte = static_cast<uint32_t>(e + 127);
-    }
-    if (real) codes[(bh * N + n) * 16 + l] = word;
-    uint32_t sw = sbyte << (8 * (l >> 2));
-    sw |= __shfl_xor_sync(0xffffffffu, sw, 4);
-    sw |= __shfl_xor_sync(0xffffffffu, sw, 8);
     if (in_range && l == 0) {
       const int64_t t = n / kTile;
       const int r = static_cast<int>(n - t * kTile);
@@ -222,11 +277,11 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       int rotate, cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);
-  const int64_t pairs = ceil_div(BH * NT * kTile, 2);
+  const int64_t groups = ceil_div(BH * NT * kTile, 32 / kQkLanesPerToken);  // one warp-iteration each
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = ceil_div(pairs, kQkThreads / 32);
+  const int64_t want = ceil_div(groups, kQkThreads / 32);
   const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
   rotate_quantize_qk_kernel<<<grid, kQkThreads, 0, s>>>(static_cast<const uint4*>(x),
                                                         static_cast<uint32_t*>(codes),
