@@ -159,11 +159,17 @@ MXATTN_API mxattn_status mxattn_forward_ex(const void* q_codes, const void* q_sc
 MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);
 
 /* The whole forward from host memory: copies q/k/v (bf16 [B,H,N,128], host;
- * page-locked memory gives full copy bandwidth) into `workspace` (device,
- * >= mxattn_workspace_bytes, 256-byte aligned), runs
- * mxattn_rotate_quantize_qk (Q and K), mxattn_quantize_v and mxattn_forward,
- * copies the fp32 result to out_host, and synchronizes `stream` before
- * returning, so out_host is ready on MXATTN_OK. */
+ * page-locked memory gives full copy bandwidth and lets the copies overlap
+ * the kernels) into `workspace` (device, >= mxattn_workspace_bytes, 256-byte
+ * aligned), runs mxattn_rotate_quantize_qk (Q and K), mxattn_quantize_v and
+ * mxattn_forward, copies the fp32 result to out_host, and synchronizes
+ * `stream` before returning, so out_host is ready on MXATTN_OK.
+ * The B*H heads run as up to 16 chunks: each chunk's copy in, kernels and
+ * copy out are ordered by events, with the copies on two internal streams
+ * and the kernels alternating between `stream` and a third internal stream
+ * (all created on the first call on a device and kept). The copies start
+ * after the work already queued on `stream`. Calls on the same device from
+ * several host threads run one after the other. */
 MXATTN_API mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, const void* v_host, int64_t B, int64_t H,
                                     int64_t N, int64_t D, int causal, float* out_host, void* workspace,
                                     size_t workspace_bytes, void* stream);

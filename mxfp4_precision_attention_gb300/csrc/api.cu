@@ -148,6 +148,46 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   return MXATTN_OK;
 }
 
+// Internal copy streams and events of mxattn_attention_host, created once per
+// device and reused; a call holds the device's lock while it enqueues and
+// waits, so concurrent host calls on one device run one after the other.
+constexpr int64_t kHostChunks = 16;
+struct HostPipe {
+  std::mutex mu;
+  cudaStream_t h2d = nullptr, d2h = nullptr, alt = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_out[kHostChunks] = {};
+  bool ready = false;
+};
+
+HostPipe* host_pipe_for_current_device(cudaError_t* err) {
+  static HostPipe pipes[64];
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  HostPipe& p = pipes[dev];
+  if (!p.ready) {
+    if ((*err = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking)) != cudaSuccess) return nullptr;
+    if ((*err = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking)) != cudaSuccess) return nullptr;
+    if ((*err = cudaStreamCreateWithFlags(&p.alt, cudaStreamNonBlocking)) != cudaSuccess) return nullptr;
+    const unsigned fl = cudaEventDisableTiming;
+    if ((*err = cudaEventCreateWithFlags(&p.ev_start, fl)) != cudaSuccess) return nullptr;
+    if ((*err = cudaEventCreateWithFlags(&p.ev_done, fl)) != cudaSuccess) return nullptr;
+    for (int i = 0; i < kHostChunks; i++) {
+      if ((*err = cudaEventCreateWithFlags(&p.ev_in[i], fl)) != cudaSuccess) return nullptr;
+      if ((*err = cudaEventCreateWithFlags(&p.ev_out[i], fl)) != cudaSuccess) return nullptr;
+    }
+    p.ready = true;
+  }
+  return &p;
+}
+
 }  // namespace
 
 void set_last_error(const char* msg) { snprintf(t_err, sizeof t_err, "%s", msg); }
@@ -349,16 +389,59 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
   uint8_t* vc = take(v_codes(B, H, N));
   float* out = reinterpret_cast<float*>(take(f32_bytes(B, H, N)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // The heads (B*H, contiguous in every layout) are split into up to
+  // kHostChunks chunks. Chunk c's inputs are copied in on one internal
+  // stream, quantized and attended on the caller's stream (even c) or a
+  // second compute stream (odd c), and its output copied out on a third
+  // stream: the copies of neighbouring chunks overlap each other and the
+  // kernels, and one chunk's CTAs fill the SMs the previous chunk's last
+  // wave leaves idle.
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(q, q_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy q");
-  if ((e = cudaMemcpyAsync(k, k_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy k");
-  if ((e = cudaMemcpyAsync(v, v_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy v");
-  MX_TRY(mxattn_rotate_quantize_qk(q, B, H, N, D, qc, qs, stream));
-  MX_TRY(mxattn_rotate_quantize_qk(k, B, H, N, D, kc, ks, stream));
-  MX_TRY(mxattn_quantize_v(v, B, H, N, D, vc, vs, stream));
-  MX_TRY(mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, D, causal, out, stream));
-  if ((e = cudaMemcpyAsync(out_host, out, f32_bytes(B, H, N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-    return cuda_fail(e, "copy out");
+  HostPipe* hp = host_pipe_for_current_device(&e);
+  if (hp == nullptr) return cuda_fail(e, "host copy streams");
+  std::lock_guard<std::mutex> lock(hp->mu);
+  const int64_t BH = B * H;
+  const int64_t nchunks = BH < kHostChunks ? BH : kHostChunks;
+  const int64_t per = ceil_div(BH, nchunks);
+  const int64_t NT = ceil_div(N, kTile), npad_half = ceil_div(N, kBlock) * kBlock / 2;
+  const size_t xh = static_cast<size_t>(N) * kD * 2, oh = static_cast<size_t>(N) * kD * 4;
+  const size_t qch = static_cast<size_t>(N) * 64, sfh = static_cast<size_t>(NT) * kSfAtomBytes,
+               vch = static_cast<size_t>(kD) * npad_half;
+  // copies into the workspace may start once earlier work on `stream` is done
+  if ((e = cudaEventRecord(hp->ev_start, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+  const char* hq = static_cast<const char*>(q_host);
+  const char* hk = static_cast<const char*>(k_host);
+  const char* hv = static_cast<const char*>(v_host);
+  char* ho = reinterpret_cast<char*>(out_host);
+  for (int64_t c = 0; c < nchunks; c++) {
+    const int64_t h0 = c * per, hn = (BH - h0) < per ? (BH - h0) : per;
+    if (hn <= 0) break;
+    const size_t xo = h0 * xh, xn = hn * xh;
+    if ((e = cudaMemcpyAsync(q + xo, hq + xo, xn, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) return cuda_fail(e, "copy q");
+    if ((e = cudaMemcpyAsync(k + xo, hk + xo, xn, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) return cuda_fail(e, "copy k");
+    if ((e = cudaMemcpyAsync(v + xo, hv + xo, xn, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) return cuda_fail(e, "copy v");
+    if ((e = cudaEventRecord(hp->ev_in[c], hp->h2d)) != cudaSuccess) return cuda_fail(e, "event record");
+    cudaStream_t cs = (c & 1) ? hp->alt : s;
+    void* cstream = static_cast<void*>(cs);
+    if ((e = cudaStreamWaitEvent(cs, hp->ev_in[c], 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+    uint8_t *cq = qc + h0 * qch, *ck = kc + h0 * qch, *cv = vc + h0 * vch;
+    uint8_t *sq = qs + h0 * sfh, *sk = ks + h0 * sfh, *sv = vs + h0 * sfh;
+    MX_TRY(mxattn_rotate_quantize_qk(q + xo, 1, hn, N, D, cq, sq, cstream));
+    MX_TRY(mxattn_rotate_quantize_qk(k + xo, 1, hn, N, D, ck, sk, cstream));
+    MX_TRY(mxattn_quantize_v(v + xo, 1, hn, N, D, cv, sv, cstream));
+    float* co = reinterpret_cast<float*>(reinterpret_cast<char*>(out) + h0 * oh);
+    MX_TRY(mxattn_forward(cq, sq, ck, sk, cv, sv, v + xo, 1, hn, N, D, causal, co, cstream));
+    if ((e = cudaEventRecord(hp->ev_out[c], cs)) != cudaSuccess) return cuda_fail(e, "event record");
+    if ((e = cudaStreamWaitEvent(hp->d2h, hp->ev_out[c], 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+    if ((e = cudaMemcpyAsync(ho + h0 * oh, co, hn * oh, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)
+      return cuda_fail(e, "copy out");
+  }
+  // `stream` is complete once the last output copy has landed (every chunk's
+  // kernels, on either compute stream, precede its output copy)
+  if ((e = cudaEventRecord(hp->ev_done, hp->d2h)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = cudaStreamWaitEvent(s, hp->ev_done, 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
   return MXATTN_OK;
 }
