@@ -40,9 +40,9 @@ FP4_OVER_BF16_NOMINAL = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rate on G
 # of the kernel source it was taken on. `traffic` is reported (scaled by B*H)
 # only while the source still has that fingerprint; otherwise it is null.
 FWD_TRAFFIC_CAPTURE = {
-    "fingerprint": "389a5249f5a4fc44",
+    "fingerprint": "d7b284cf8ea4b985",
     "bh": 8, "n": 32760,
-    "read_bytes": 53530624, "write_bytes": 79385856,
+    "read_bytes": 53529088, "write_bytes": 79088640,
 }
 FWD_SOURCES = ("attn_mxfp4.cu", "sm103_ptx.cuh", "internal.h")
 
@@ -294,6 +294,24 @@ def run_ours(args, w):
     qk_bytes = 2 * (e * 2 + mx.qk_layout_sizes(B, H, N)[0] + mx.qk_layout_sizes(B, H, N)[1])
     v_bytes = e * 2 + vcn + vsn
 
+    # the BF16 comparison path on the same inputs (not part of the step)
+    bf16_path = None
+    if not args.no_bf16:
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                mx.mxattn_forward_bf16(q, k, v, causal=w.causal, out=out, stream=stream)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(3):
+                mx.mxattn_forward_bf16(q, k, v, causal=w.causal, out=out, stream=stream)
+            b1.record(stream)
+        torch.cuda.synchronize()
+        mx.mxattn_check(stream)
+        bms = b0.elapsed_time(b1) / 3
+        bt = flops / (bms * 1e-3) / 1e12
+        bf16_path = {"kernel": "bf16_fwd_kernel (tcgen05 kind::f16)", "ms": bms, "tflops": bt,
+                     "frac_of_bf16_peak": bt / bf16, "mxfp4_speedup": bms / fwd_ms}
+
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
     if not args.no_e2e:
@@ -346,6 +364,7 @@ def run_ours(args, w):
             "quantizer_gbs": {"qk": qk_bytes / (qk_ms * 1e-3) / 1e9, "v": v_bytes / (v_ms * 1e-3) / 1e9,
                               "hbm_peak": hbm},
             "gpu_launches": 4 * args.steps,
+            "bf16_path": bf16_path,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -441,6 +460,7 @@ def main():
     ap.add_argument("--n", type=int, default=None, help="override N (smaller profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison-path timing")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--accuracy", action="store_true",

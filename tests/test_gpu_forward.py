@@ -249,13 +249,13 @@ def test_host_entry_point_matches_device_path(mx):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_host_entry_point_pipelined_chunks(mx, causal):
-    """14 heads run as 7 chunks whose copies overlap the kernels; two calls in a
-    row (the internal streams and events are reused) give the device path's
-    output bit for bit."""
-    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=2, H=7, N=300, seed=17)
+    """21 heads run as 11 chunks of two heads (the last holds one) whose copies
+    overlap the kernels; two calls in a row (the internal streams and events
+    are reused) give the device path's output bit for bit."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=3, H=7, N=300, seed=17)
     dev = _gpu_mx(mx, q, k, v, causal=causal).cpu()
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    ws = torch.empty(mx.mxattn_workspace_bytes(2, 7, 300), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(mx.mxattn_workspace_bytes(3, 7, 300), dtype=torch.uint8, device="cuda")
     for _ in range(2):
         outh = torch.full(q.shape, float("nan"), dtype=torch.float32).pin_memory()
         mx.mxattn_attention_host(qh, kh, vh, causal, outh, ws)
