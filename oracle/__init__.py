@@ -15,7 +15,8 @@ All layouts here are *logical*: codes one per byte, scales as biased E8M0
 bytes (e + 127), Q/K scales ``[rows, 4]``, V codes ``[BH, N, 128]`` token-major
 and V scales ``[BH, 128, ceil(N/32)]``.
 
-Scale rules: 0 = UOS (ceil, Q_max = 7.25), 1 = OCP floor, 2 = TFS (ceil, 6).
+Scale rules: 0 = UOS (ceil, Q_max = 7.25), 1 = OCP floor, 2 = TFS (ceil, 6),
+3 = ceil with a given Q_max q in (4, 8] (the Q_max sweep of section 5.5.1).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against values and identities the pages fix (see the header of each test).
@@ -35,7 +36,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-UOS, OCP, TFS = 0, 1, 2
+UOS, OCP, TFS, CEIL_Q = 0, 1, 2, 3
 PNQ, DIRECT = 0, 1
 D = 128
 BLOCK = 32
@@ -69,13 +70,16 @@ def _load():
             lib.orc_e2m1_code.restype = I
             lib.orc_scale_exponent.argtypes = [ctypes.c_double, I]
             lib.orc_scale_exponent.restype = I
+            lib.orc_scale_exponent_q.argtypes = [ctypes.c_double, I, ctypes.c_double]
+            lib.orc_scale_exponent_q.restype = I
             lib.orc_uos_qmax.argtypes = []
             lib.orc_uos_qmax.restype = ctypes.c_double
             lib.orc_hadamard_fp32.argtypes = [P, P]
-            lib.orc_rotate_quantize_qk.argtypes = [P, I64, I, I, P, P]
-            lib.orc_quantize_v.argtypes = [P, I64, I64, I, P, P]
-            lib.orc_online_softmax.argtypes = [P, P, I64, P, P, P, I64, I, I, I, I, I, P, P, P, P]
-            lib.orc_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I, I, I, I, I, P, I64, P, P, P, P]
+            Dbl = ctypes.c_double
+            lib.orc_rotate_quantize_qk.argtypes = [P, I64, I, Dbl, I, P, P]
+            lib.orc_quantize_v.argtypes = [P, I64, I64, I, Dbl, P, P]
+            lib.orc_online_softmax.argtypes = [P, P, I64, P, P, P, I64, I, I, I, I, Dbl, I, P, P, P, P]
+            lib.orc_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I, I, I, Dbl, I, I, P, I64, P, P, P, P]
             lib.orc_forward.restype = I
             lib.orc_sdpa.argtypes = [P, P, P, I64, I64, I, P, I64, P]
             lib.orc_num_threads.restype = I
@@ -114,8 +118,9 @@ def e2m1_code(v) -> np.ndarray:
     return out
 
 
-def scale_exponent(M: float, rule: int = UOS) -> int:
-    return int(_load().orc_scale_exponent(float(M), int(rule)))
+def scale_exponent(M: float, rule: int = UOS, q: float = 7.25) -> int:
+    """Block scale exponent of a maximum M > 0 under `rule` (q is used by CEIL_Q)."""
+    return int(_load().orc_scale_exponent_q(float(M), int(rule), float(q)))
 
 
 def hadamard_fp32(x_u16: np.ndarray) -> np.ndarray:
@@ -128,7 +133,7 @@ def hadamard_fp32(x_u16: np.ndarray) -> np.ndarray:
     return y.reshape(np.shape(x_u16))
 
 
-def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True):
+def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True, q: float = 7.25):
     """Algorithm 2 (section 4.3), the rotation and Q/K quantization steps. ``x_u16``: bf16 bits ``[..., 128]``.
 
     Returns (codes ``[..., 128]`` uint8, scales ``[..., 4]`` uint8)."""
@@ -137,12 +142,12 @@ def rotate_quantize_qk(x_u16: np.ndarray, rule: int = UOS, rotate: bool = True):
     rows = x.shape[0]
     codes = np.empty((rows, D), dtype=np.uint8)
     scales = np.empty((rows, D // BLOCK), dtype=np.uint8)
-    lib.orc_rotate_quantize_qk(_p(x), rows, int(rule), int(bool(rotate)), _p(codes), _p(scales))
+    lib.orc_rotate_quantize_qk(_p(x), rows, int(rule), float(q), int(bool(rotate)), _p(codes), _p(scales))
     lead = np.shape(x_u16)[:-1]
     return codes.reshape(*lead, D), scales.reshape(*lead, D // BLOCK)
 
 
-def quantize_v(v_u16: np.ndarray, rule: int = UOS):
+def quantize_v(v_u16: np.ndarray, rule: int = UOS, q: float = 7.25):
     """Algorithm 2 (section 4.3), the V quantization step, on ``[BH, N, 128]`` bf16 bits.
 
     Returns (codes ``[BH, N, 128]``, scales ``[BH, 128, ceil(N/32)]``)."""
@@ -152,12 +157,12 @@ def quantize_v(v_u16: np.ndarray, rule: int = UOS):
     nblk = (N + BLOCK - 1) // BLOCK
     codes = np.empty((BH, N, D), dtype=np.uint8)
     scales = np.empty((BH, D, nblk), dtype=np.uint8)
-    lib.orc_quantize_v(_p(v), BH, N, int(rule), _p(codes), _p(scales))
+    lib.orc_quantize_v(_p(v), BH, N, int(rule), float(q), _p(codes), _p(scales))
     return codes, scales
 
 
 def online_softmax(q_rows, row_tok, K, V, Vraw=None, *, causal=False, quant_p=True, placement=PNQ,
-                   p_rule=UOS, bc=BC, want_phat=False):
+                   p_rule=UOS, p_q=7.25, bc=BC, want_phat=False):
     """Algorithm 2 (section 4.3), the tiled online-softmax loop (Eqs. 2-8, 44-48), on real-valued inputs (float64).
 
     ``q_rows``: ``[R, 128]``; ``row_tok``: token index of each row; ``K, V``:
@@ -177,7 +182,7 @@ def online_softmax(q_rows, row_tok, K, V, Vraw=None, *, causal=False, quant_p=Tr
     phat = np.zeros((R, ntiles * bc)) if want_phat else None
     mhist = np.full((R, ntiles), np.nan) if want_phat else None
     lib.orc_online_softmax(_p(q), _p(tok), R, _p(K), _p(V), _p(Vr), N, int(causal), int(quant_p),
-                           int(placement), int(p_rule), int(bc), _p(out), _p(ell), _p(phat), _p(mhist))
+                           int(placement), int(p_rule), float(p_q), int(bc), _p(out), _p(ell), _p(phat), _p(mhist))
     res = {"out": out, "ell": ell}
     if want_phat:
         res["phat"] = phat
@@ -186,7 +191,7 @@ def online_softmax(q_rows, row_tok, K, V, Vraw=None, *, causal=False, quant_p=Tr
 
 
 def forward(qc, qs, kc, ks, vc, vs, rows, *, vraw_u16=None, causal=False, placement=PNQ, p_rule=UOS,
-            quant_p=True, bc=BC, want_phat=False):
+            p_q=7.25, quant_p=True, bc=BC, want_phat=False):
     """Alg. 2 on quantized tensors in the oracle's logical layouts.
 
     ``rows``: ``[R, 2]`` int array of (bh, token). Returns dict as
@@ -210,7 +215,7 @@ def forward(qc, qs, kc, ks, vc, vs, rows, *, vraw_u16=None, causal=False, placem
     phat = np.zeros((R, ntiles * bc)) if want_phat else None
     mhist = np.full((R, ntiles), np.nan) if want_phat else None
     rc = lib.orc_forward(_p(qc), _p(qs), _p(kc), _p(ks), _p(vc), _p(vs), _p(vr), BH, N, int(causal),
-                         int(placement), int(p_rule), int(quant_p), int(bc), _p(rows), R, _p(out), _p(ell),
+                         int(placement), int(p_rule), float(p_q), int(quant_p), int(bc), _p(rows), R, _p(out), _p(ell),
                          _p(phat), _p(mhist))
     if rc != 0:
         raise RuntimeError(f"orc_forward failed with code {rc}")

@@ -69,30 +69,36 @@ int orc_e2m1_code(double v) {
  * rule 0: UOS, e = ceil(log2(M / 7.25))           (Eq. 13 / 19, Alg. 1)
  * rule 1: OCP, e = floor(log2 M) - 2              (Eq. 11 / 97)
  * rule 2: TFS, e = ceil(log2(M / 6))              (Eq. 14)
+ * rule 3: e = ceil(log2(M / q)) for a given q in (4, 8]: the Q_max sweep of
+ *         section 5.5.1 (q = 7.25 is UOS, q = 6 is TFS)
  * M > 0. With M = f * 2^E, f in [0.5, 1):
- *   ceil(log2(M/q)) = E - 3 if f <= q/8 else E - 2, for q in (4, 8];
+ *   ceil(log2(M/q)) = E - 3 if f <= q/8 else E - 2, for q in (4, 8]
+ *   (and E - 4 if f <= q/16, which needs q = 8 and f = 1/2);
  *   floor(log2 M)   = E - 1.
  * Result clamped to the E8M0 exponent range [-127, 127].                   */
 double orc_uos_qmax(void) { return 7.25; }
 
-int orc_scale_exponent(double M, int rule) {
+int orc_scale_exponent_q(double M, int rule, double qmax) {
   int E;
   double f = frexp(M, &E);
   int e;
   if (rule == 1) {
     e = (E - 1) - 2;
   } else {
-    double q = (rule == 2) ? 6.0 : orc_uos_qmax();
-    e = (f <= q / 8.0) ? E - 3 : E - 2;
+    double q = (rule == 2) ? 6.0 : (rule == 3 ? qmax : orc_uos_qmax());
+    /* smallest e with M / 2^e <= q; f <= q/16 happens only for q = 8, f = 1/2 */
+    e = (f <= q / 16.0) ? E - 4 : ((f <= q / 8.0) ? E - 3 : E - 2);
   }
   if (e < -127) e = -127;
   if (e > 127) e = 127;
   return e;
 }
 
+int orc_scale_exponent(double M, int rule) { return orc_scale_exponent_q(M, rule, 7.25); }
+
 /* Quantize one block of n values (Algorithm 1). codes[i] receives the 4-bit
  * code, the return value is the biased E8M0 byte.                          */
-static int quantize_block(const double* v, int n, int rule, uint8_t* codes) {
+static int quantize_block(const double* v, int n, int rule, double q, uint8_t* codes) {
   double M = 0.0;
   for (int i = 0; i < n; i++) {
     double a = fabs(v[i]);
@@ -102,7 +108,7 @@ static int quantize_block(const double* v, int n, int rule, uint8_t* codes) {
     for (int i = 0; i < n; i++) codes[i] = 0;
     return 127;
   }
-  int e = orc_scale_exponent(M, rule);
+  int e = orc_scale_exponent_q(M, rule, q);
   for (int i = 0; i < n; i++) codes[i] = (uint8_t)orc_e2m1_code(ldexp(v[i], -e));
   return e + 127;
 }
@@ -140,7 +146,7 @@ void orc_hadamard_fp32(const uint16_t* x_bf16, float* y) {
 /* ------------------------------------------------- Q / K quantization
  * Algorithm 2 (section 4.3), Q/K steps: rotate each token, then quantize each 32-channel block.
  * codes: rows x 128 (one code per byte); scales: rows x 4 biased bytes.    */
-void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotate, uint8_t* codes,
+void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, double q, int rotate, uint8_t* codes,
                             uint8_t* scales) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; r++) {
@@ -153,7 +159,7 @@ void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotat
     for (int b = 0; b < ORC_D / ORC_BLOCK; b++) {
       double v[ORC_BLOCK];
       for (int i = 0; i < ORC_BLOCK; i++) v[i] = (double)y[b * ORC_BLOCK + i];
-      scales[r * 4 + b] = (uint8_t)quantize_block(v, ORC_BLOCK, rule, codes + r * ORC_D + b * ORC_BLOCK);
+      scales[r * 4 + b] = (uint8_t)quantize_block(v, ORC_BLOCK, rule, q, codes + r * ORC_D + b * ORC_BLOCK);
     }
   }
 }
@@ -162,7 +168,7 @@ void orc_rotate_quantize_qk(const uint16_t* x, int64_t rows, int rule, int rotat
  * Algorithm 2 (section 4.3), V step, with token blocks (R4). v: [BH][N][128] bf16.
  * codes: [BH][N][128] (token-major, one code per byte);
  * scales: [BH][128][nblk], nblk = ceil(N/32).                              */
-void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, uint8_t* codes, uint8_t* scales) {
+void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, double q, uint8_t* codes, uint8_t* scales) {
   const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t bh = 0; bh < BH; bh++) {
@@ -173,7 +179,7 @@ void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, uint8_t*
         double vals[ORC_BLOCK];
         uint8_t cb[ORC_BLOCK];
         for (int i = 0; i < n; i++) vals[i] = (double)bf16_to_f32(v[((bh * N) + n0 + i) * ORC_D + c]);
-        scales[(bh * ORC_D + c) * nblk + t] = (uint8_t)quantize_block(vals, n, rule, cb);
+        scales[(bh * ORC_D + c) * nblk + t] = (uint8_t)quantize_block(vals, n, rule, q, cb);
         for (int i = 0; i < n; i++) codes[((bh * N) + n0 + i) * ORC_D + c] = cb[i];
       }
     }
@@ -197,6 +203,7 @@ typedef struct {
   int placement;
   int p_rule;
   int bc;
+  double p_q;
 } orc_opts;
 
 static void online_softmax_row(const double* q, const double* K, const double* V, const double* Vraw,
@@ -238,7 +245,7 @@ static void online_softmax_row(const double* q, const double* K, const double* V
     for (int b0 = 0; b0 < bc; b0 += ORC_BLOCK) {
       if (op->quant_p) {
         uint8_t cb[ORC_BLOCK];
-        int sb = quantize_block(Pt + b0, ORC_BLOCK, op->p_rule, cb);
+        int sb = quantize_block(Pt + b0, ORC_BLOCK, op->p_rule, op->p_q, cb);
         for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = dq(cb[t], (uint8_t)sb);
       } else {
         for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = Pt[b0 + t];
@@ -275,9 +282,9 @@ static void online_softmax_row(const double* q, const double* K, const double* V
  * K, V, Vraw: N x 128 (Vraw may be NULL when not causal).                   */
 void orc_online_softmax(const double* q_rows, const int64_t* row_tok, int64_t nrows, const double* K,
                         const double* V, const double* Vraw, int64_t N, int causal, int quant_p,
-                        int placement, int p_rule, int bc, double* out, double* ell, double* phat,
+                        int placement, int p_rule, double p_q, int bc, double* out, double* ell, double* phat,
                         double* mhist) {
-  orc_opts op = {causal, quant_p, placement, p_rule, bc};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q};
   const int64_t ntiles = (N + bc - 1) / bc;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; r++) {
@@ -296,12 +303,12 @@ void orc_online_softmax(const double* q_rows, const int64_t* row_tok, int64_t nr
  * Rows are grouped by head by the caller for efficiency (not required).     */
 int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const uint8_t* ks, const uint8_t* vc,
                 const uint8_t* vs, const uint16_t* vraw, int64_t BH, int64_t N, int causal, int placement,
-                int p_rule, int quant_p, int bc, const int64_t* rows, int64_t nrows, double* out, double* ell,
-                double* phat, double* mhist) {
+                int p_rule, double p_q, int quant_p, int bc, const int64_t* rows, int64_t nrows, double* out,
+                double* ell, double* phat, double* mhist) {
   if (bc <= 0 || bc % ORC_BLOCK != 0) return 1;
   const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
   const int64_t ntiles = (N + bc - 1) / bc;
-  orc_opts op = {causal, quant_p, placement, p_rule, bc};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q};
   double* K = (double*)malloc(sizeof(double) * N * ORC_D);
   double* V = (double*)malloc(sizeof(double) * N * ORC_D);
   double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);

@@ -165,3 +165,23 @@ def test_v_token_blocks_and_short_tail(orc):
     # dequantized spike is within one grid step
     deq = orc.dequant_v(codes, scales)
     assert abs(deq[0, 40, 9] - vf[0, 40, 9]) <= 0.5 * 2.0 ** (int(scales[0, 9, 1]) - 127) * 2 + 1e-12
+
+
+def test_ceil_q_rule_defines_the_qmax_sweep(orc):
+    """Section 5.5.1 sweeps Q_max over [6.00, 8.00] in steps of 0.05: e = ceil(log2(M / q))
+    is the smallest exponent that brings the block maximum to at most q, so the
+    normalized maximum lies in (q/2, q]; exact boundaries M = q * 2^k give e = k and one
+    ulp above gives k + 1. q = 7.25 is UOS and q = 6 is TFS."""
+    rng = np.random.default_rng(11)
+    M = np.exp2(rng.uniform(-40, 40, 100000))
+    for q in np.round(np.arange(6.0, 8.0001, 0.05), 2):
+        e = np.array([orc.scale_exponent(m, orc.CEIL_Q, q) for m in M[:4000]])
+        x = M[:4000] / np.exp2(e)
+        assert np.all(x <= q) and np.all(x > q / 2), q
+        for k in (-20, -3, 0, 5, 30):
+            b = q * 2.0 ** k
+            assert orc.scale_exponent(b, orc.CEIL_Q, q) == k
+            assert orc.scale_exponent(np.nextafter(b, np.inf), orc.CEIL_Q, q) == k + 1
+    for m in M[:20000:7]:
+        assert orc.scale_exponent(m, orc.CEIL_Q, 7.25) == orc.scale_exponent(m, orc.UOS)
+        assert orc.scale_exponent(m, orc.CEIL_Q, 6.0) == orc.scale_exponent(m, orc.TFS)
