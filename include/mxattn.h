@@ -132,6 +132,9 @@ MXATTN_API mxattn_status mxattn_forward_bf16(const void* q, const void* k, const
  *               MXATTN_RULE_UOS: e = ceil(log2(M / 7.25))   (Eq. 13, Algorithm 1)
  *               MXATTN_RULE_OCP: e = floor(log2 M) - 2      (Eq. 11; maxima in [4, 8), above 6 saturate)
  *               MXATTN_RULE_TFS: e = ceil(log2(M / 6))      (Eq. 14)
+ *               MXATTN_RULE_CEIL: e = ceil(log2(M / qmax)), qmax in (4, 8]: the
+ *                                 Q_max sweep of section 5.5.1 (7.25 is UOS,
+ *                                 6 is TFS); qmax is ignored by the other rules
  *               All-zero blocks take sigma = 1 under every rule; e is
  *               clamped to [-127, 127] as for UOS.
  *   rotate    : 1 = fixed Hadamard rotation as in mxattn_rotate_quantize_qk,
@@ -144,16 +147,16 @@ MXATTN_API mxattn_status mxattn_forward_bf16(const void* q, const void* k, const
  * rotate = 1 and placement = PNQ they compute exactly what
  * mxattn_rotate_quantize_qk, mxattn_quantize_v and mxattn_forward compute.
  * Q and K must share `rotate` (rotating only one changes S). */
-typedef enum { MXATTN_RULE_UOS = 0, MXATTN_RULE_OCP = 1, MXATTN_RULE_TFS = 2 } mxattn_scale_rule;
+typedef enum { MXATTN_RULE_UOS = 0, MXATTN_RULE_OCP = 1, MXATTN_RULE_TFS = 2, MXATTN_RULE_CEIL = 3 } mxattn_scale_rule;
 typedef enum { MXATTN_PLACE_PNQ = 0, MXATTN_PLACE_DIRECT = 1 } mxattn_placement;
 MXATTN_API mxattn_status mxattn_quantize_qk_ex(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, int rule,
-                                               int rotate, void* codes, void* scales, void* stream);
+                                               double qmax, int rotate, void* codes, void* scales, void* stream);
 MXATTN_API mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, int rule,
-                                              void* codes, void* scales, void* stream);
+                                              double qmax, void* codes, void* scales, void* stream);
 MXATTN_API mxattn_status mxattn_forward_ex(const void* q_codes, const void* q_scales, const void* k_codes,
                                            const void* k_scales, const void* v_codes, const void* v_scales,
                                            const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
-                                           int p_rule, int placement, float* out, void* stream);
+                                           int p_rule, double p_qmax, int placement, float* out, void* stream);
 
 /* Device workspace needed by mxattn_attention_host for [B, H, N, 128]. */
 MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);

@@ -59,9 +59,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
-        lib.mxattn_quantize_qk_ex.argtypes = [P, I64, I64, I64, I64, I, I, P, P, P]
-        lib.mxattn_quantize_v_ex.argtypes = [P, I64, I64, I64, I64, I, P, P, P]
-        lib.mxattn_forward_ex.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, I, P, P]
+        Dbl = ctypes.c_double
+        lib.mxattn_quantize_qk_ex.argtypes = [P, I64, I64, I64, I64, I, Dbl, I, P, P, P]
+        lib.mxattn_quantize_v_ex.argtypes = [P, I64, I64, I64, I64, I, Dbl, P, P, P]
+        lib.mxattn_forward_ex.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, Dbl, I, P, P]
         lib.mxattn_attention_host.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, SZ, P]
         lib.mxattn_attention_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_attention_noalloc.restype = I
@@ -159,42 +160,44 @@ def mxattn_forward_dump_phat(q_codes, q_scales, k_codes, k_scales, v_codes, v_sc
 
 
 # Ablation switches (include/mxattn.h: mxattn_scale_rule, mxattn_placement)
-RULE_UOS, RULE_OCP, RULE_TFS = 0, 1, 2
+RULE_UOS, RULE_OCP, RULE_TFS, RULE_CEIL = 0, 1, 2, 3
 PLACE_PNQ, PLACE_DIRECT = 0, 1
 
 
-def mxattn_quantize_qk_ex(x: torch.Tensor, rule: int = RULE_UOS, rotate: bool = True,
+def mxattn_quantize_qk_ex(x: torch.Tensor, rule: int = RULE_UOS, rotate: bool = True, qmax: float = 7.25,
                           codes: torch.Tensor | None = None, scales: torch.Tensor | None = None, stream=None):
-    """Q/K quantization with a chosen scale rule and optional rotation. Returns (codes, scales)."""
+    """Q/K quantization with a chosen scale rule (qmax for RULE_CEIL) and optional rotation.
+    Returns (codes, scales)."""
     B, H, N, Dx = _shape(x)
     nc, ns = qk_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=x.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=x.device) if scales is None else scales
-    _raise(load().mxattn_quantize_qk_ex(_ptr(x), B, H, N, Dx, int(rule), int(bool(rotate)), _ptr(codes),
-                                        _ptr(scales), _stream(stream)))
+    _raise(load().mxattn_quantize_qk_ex(_ptr(x), B, H, N, Dx, int(rule), float(qmax), int(bool(rotate)),
+                                        _ptr(codes), _ptr(scales), _stream(stream)))
     return codes, scales
 
 
-def mxattn_quantize_v_ex(v: torch.Tensor, rule: int = RULE_UOS, codes: torch.Tensor | None = None,
+def mxattn_quantize_v_ex(v: torch.Tensor, rule: int = RULE_UOS, qmax: float = 7.25, codes: torch.Tensor | None = None,
                          scales: torch.Tensor | None = None, stream=None):
-    """V quantization with a chosen scale rule. Returns (codes, scales)."""
+    """V quantization with a chosen scale rule (qmax for RULE_CEIL). Returns (codes, scales)."""
     B, H, N, Dx = _shape(v)
     nc, ns = v_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=v.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
-    _raise(load().mxattn_quantize_v_ex(_ptr(v), B, H, N, Dx, int(rule), _ptr(codes), _ptr(scales), _stream(stream)))
+    _raise(load().mxattn_quantize_v_ex(_ptr(v), B, H, N, Dx, int(rule), float(qmax), _ptr(codes), _ptr(scales),
+                                       _stream(stream)))
     return codes, scales
 
 
 def mxattn_forward_ex(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
                       causal: bool = False, p_rule: int = RULE_UOS, placement: int = PLACE_PNQ,
-                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                      p_qmax: float = 7.25, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Forward with the P~ scale rule and the l placement as switches. Returns fp32 [B, H, N, 128]."""
     dev = q_codes.device
     out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
     _raise(load().mxattn_forward_ex(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
                                     _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), int(p_rule),
-                                    int(placement), _ptr(out), _stream(stream)))
+                                    float(p_qmax), int(placement), _ptr(out), _stream(stream)))
     return out
 
 

@@ -93,10 +93,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
+mxattn_status check_rule(int rule, double qmax, const char* what) {
+  if (rule < kRuleUOS || rule > kRuleCeilQ)
+    return fail(MXATTN_ERR_INVALID_ARG, "%s must be 0 (UOS), 1 (OCP), 2 (TFS) or 3 (ceil with qmax)", what);
+  if (rule == kRuleCeilQ && !(qmax > 4.0 && qmax <= 8.0))
+    return fail(MXATTN_ERR_INVALID_ARG, "qmax must lie in (4, 8] for the ceil rule");
+  return MXATTN_OK;
+}
+
 mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                            const void* vs, const void* vb, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                            float* out, uint8_t* pc, uint8_t* ps, void* stream, int p_rule = kRuleUOS,
-                           int placement = kPlacePNQ) {
+                           int placement = kPlacePNQ, double p_qmax = 7.25) {
   bool empty = false;
   MX_TRY(check_shape(B, H, N, D, &empty));
   if (empty) return MXATTN_OK;
@@ -108,7 +116,7 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   MX_TRY(check_ptr(vs, "v_scales"));
   MX_TRY(check_ptr(out, "out"));
   if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
-  if (p_rule < kRuleUOS || p_rule > kRuleTFS) return fail(MXATTN_ERR_INVALID_ARG, "p_rule must be 0 (UOS), 1 (OCP) or 2 (TFS)");
+  MX_TRY(check_rule(p_rule, p_qmax, "p_rule"));
   if (placement != kPlacePNQ && placement != kPlaceDirect)
     return fail(MXATTN_ERR_INVALID_ARG, "placement must be 0 (PNQ) or 1 (direct)");
   if (causal) MX_TRY(check_ptr(vb, "v_bf16 (required when causal)"));
@@ -141,6 +149,7 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   a.debug_flags = g_debug_flags;
   a.p_rule = p_rule;
   a.placement = placement;
+  a.p_qmax = p_qmax;
   if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
   cudaError_t e = launch_mxfp4_forward(a, static_cast<cudaStream_t>(stream));
@@ -252,13 +261,13 @@ size_t mxattn_v_scales_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || 
 
 mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
                                         void* scales, void* stream) {
-  return mxattn_quantize_qk_ex(x, B, H, N, D, MXATTN_RULE_UOS, 1, codes, scales, stream);
+  return mxattn_quantize_qk_ex(x, B, H, N, D, MXATTN_RULE_UOS, 7.25, 1, codes, scales, stream);
 }
 
-mxattn_status mxattn_quantize_qk_ex(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, int rule, int rotate,
-                                    void* codes, void* scales, void* stream) {
+mxattn_status mxattn_quantize_qk_ex(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, int rule,
+                                    double qmax, int rotate, void* codes, void* scales, void* stream) {
   t_err[0] = '\0';
-  if (rule < kRuleUOS || rule > kRuleTFS) return fail(MXATTN_ERR_INVALID_ARG, "rule must be 0 (UOS), 1 (OCP) or 2 (TFS)");
+  MX_TRY(check_rule(rule, qmax, "rule"));
   if (rotate != 0 && rotate != 1) return fail(MXATTN_ERR_INVALID_ARG, "rotate must be 0 or 1");
   bool empty = false;
   MX_TRY(check_shape(B, H, N, D, &empty));
@@ -269,20 +278,21 @@ mxattn_status mxattn_quantize_qk_ex(const void* x, int64_t B, int64_t H, int64_t
   const Range rx = rng(x, bf16_bytes(B, H, N)), rc = rng(codes, qk_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
   if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs))
     return fail(MXATTN_ERR_INVALID_ARG, "x, codes and scales must not overlap");
-  cudaError_t e = launch_rotate_quantize_qk(x, B * H, N, codes, scales, rule, rotate, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      launch_rotate_quantize_qk(x, B * H, N, codes, scales, rule, qmax, rotate, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_qk launch");
   return MXATTN_OK;
 }
 
 mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
                                 void* scales, void* stream) {
-  return mxattn_quantize_v_ex(v, B, H, N, D, MXATTN_RULE_UOS, codes, scales, stream);
+  return mxattn_quantize_v_ex(v, B, H, N, D, MXATTN_RULE_UOS, 7.25, codes, scales, stream);
 }
 
-mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, int rule, void* codes,
-                                   void* scales, void* stream) {
+mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, int rule, double qmax,
+                                   void* codes, void* scales, void* stream) {
   t_err[0] = '\0';
-  if (rule < kRuleUOS || rule > kRuleTFS) return fail(MXATTN_ERR_INVALID_ARG, "rule must be 0 (UOS), 1 (OCP) or 2 (TFS)");
+  MX_TRY(check_rule(rule, qmax, "rule"));
   bool empty = false;
   MX_TRY(check_shape(B, H, N, D, &empty));
   if (empty) return MXATTN_OK;
@@ -292,7 +302,7 @@ mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t 
   const Range rv = rng(v, bf16_bytes(B, H, N)), rc = rng(codes, v_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
   if (overlap(rv, rc) || overlap(rv, rs) || overlap(rc, rs))
     return fail(MXATTN_ERR_INVALID_ARG, "v, codes and scales must not overlap");
-  cudaError_t e = launch_quantize_v(v, B * H, N, codes, scales, rule, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_quantize_v(v, B * H, N, codes, scales, rule, qmax, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_v launch");
   return MXATTN_OK;
 }
@@ -318,10 +328,11 @@ mxattn_status mxattn_forward_dump_phat(const void* q_codes, const void* q_scales
 
 mxattn_status mxattn_forward_ex(const void* q_codes, const void* q_scales, const void* k_codes, const void* k_scales,
                                 const void* v_codes, const void* v_scales, const void* v_bf16, int64_t B, int64_t H,
-                                int64_t N, int64_t D, int causal, int p_rule, int placement, float* out, void* stream) {
+                                int64_t N, int64_t D, int causal, int p_rule, double p_qmax, int placement,
+                                float* out, void* stream) {
   t_err[0] = '\0';
   return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
-                      nullptr, nullptr, stream, p_rule, placement);
+                      nullptr, nullptr, stream, p_rule, placement, p_qmax);
 }
 
 mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,

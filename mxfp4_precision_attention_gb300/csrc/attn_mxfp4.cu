@@ -36,6 +36,8 @@
 // released before the CTA returns.
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "internal.h"
 #include "sm103_ptx.cuh"
 
@@ -105,6 +107,7 @@ struct Params {
   uint32_t debug_flags;
   int p_rule;     // variant kernels only
   int placement;  // variant kernels only
+  float p_log2q;  // variant kernels, kRuleCeilQ: log2(Q_max)
   float score_scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -139,7 +142,8 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
 // kCausal and kDump are compile-time so the non-causal, non-diagnostic path
 // carries no checks for either. kVariant builds the ablation variants of
 // section 5.4 (Table 3): the P~ blocks take the scale rule p.p_rule (UOS, OCP
-// floor of Eq. 11, TFS of Eq. 14) and l may come from the unquantized P~
+// floor of Eq. 11, TFS of Eq. 14, or the ceil rule with a swept Q_max of
+// section 5.5.1) and l may come from the unquantized P~
 // (direct placement, Eqs. 16-17) instead of P^ (PNQ, Eq. 47).
 template <bool kCausal, bool kDump, bool kVariant>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -425,7 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (unit spacing there), so the low byte of its bits is the E8M0 byte
       // e + 127, and kExpMagic - t recovers -e exactly.
       float qoff = kLog2Qmax;
-      if constexpr (kVariant) qoff = p.p_rule == kRuleTFS ? kLog2Six : (p.p_rule == kRuleOCP ? 2.0f : kLog2Qmax);
+      if constexpr (kVariant)
+        qoff = p.p_rule == kRuleTFS ? kLog2Six
+               : p.p_rule == kRuleOCP ? 2.0f
+               : p.p_rule == kRuleCeilQ ? p.p_log2q
+                                         : kLog2Qmax;
       const float2 nm2 = make_float2(-m_new, -m_new), nq2 = make_float2(-qoff, -qoff);
       const float2 xe01 = __ffma2_rn(__fadd2_rn(make_float2(bm[0], bm[1]), nm2), c2, nq2);
       const float2 xe23 = __ffma2_rn(__fadd2_rn(make_float2(bm[2], bm[3]), nm2), c2, nq2);
@@ -698,6 +706,7 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.debug_flags = a.debug_flags;
   p.p_rule = a.p_rule;
   p.placement = a.placement;
+  p.p_log2q = static_cast<float>(std::log2(a.p_qmax));
   p.score_scale_log2 = kLog2e / 11.313708498984761f;  // log2(e) / sqrt(128)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -17,13 +17,14 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 enum : uint32_t { kDebugNeverArriveS = 1u };
 
 // Block scale rules (same numbering as mxattn_scale_rule) and l placements.
-enum : int { kRuleUOS = 0, kRuleOCP = 1, kRuleTFS = 2 };
+enum : int { kRuleUOS = 0, kRuleOCP = 1, kRuleTFS = 2, kRuleCeilQ = 3 };
 enum : int { kPlacePNQ = 0, kPlaceDirect = 1 };
 
+// qmax is used by kRuleCeilQ only (a value in (4, 8]).
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
-                                      int rotate, cudaStream_t s);
+                                      double qmax, int rotate, cudaStream_t s);
 cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,
-                              cudaStream_t s);
+                              double qmax, cudaStream_t s);
 
 struct Mxfp4FwdArgs {
   const void* q_codes;
@@ -40,6 +41,7 @@ struct Mxfp4FwdArgs {
   uint8_t* phat_scales;  // optional diagnostic dump, [BH][N][ceil(N/128)*4]
   uint32_t debug_flags;
   int p_rule;     // scale rule of the P~ blocks (kRule*)
+  double p_qmax;  // Q_max of kRuleCeilQ
   int placement;  // kPlacePNQ: l from P^ (Eq. 47); kPlaceDirect: l from P~ (Eq. 16)
 };
 cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s);

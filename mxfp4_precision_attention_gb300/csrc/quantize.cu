@@ -22,6 +22,8 @@
 //   scale byte = e + 127 (E8M0); an all-zero block gets 127 and zero codes.
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "internal.h"
 #include "sm103_ptx.cuh"
 
@@ -34,19 +36,35 @@ constexpr float kRotScale = 0x1.6a09e6p-4f;  // binary32 nearest to 2^-3.5 = 1/s
 //   UOS  ceil(log2(M/7.25)) = (b-126) - 3 if 1.f <= 1.8125 else (b-126) - 2
 //   TFS  ceil(log2(M/6))    = (b-126) - 3 if 1.f <= 1.5    else (b-126) - 2
 //   OCP  floor(log2 M) - 2  = (b-126) - 3
+//   ceil(log2(M/q)), q in (4, 8]: (b-126) - 3 if 1.f <= q/4 else (b-126) - 2,
+//        and one lower for an exact power of two when q = 8
 // i.e. one comparison of the mantissa field against mant_thr (0x680000,
-// 0x400000, or 0x7FFFFF so that it always holds). Denormal maxima and
-// anything below the E8M0 range clamp to -127.
-__device__ __forceinline__ int block_exponent(float M, uint32_t mant_thr) {
+// 0x400000, floor((q/4 - 1) * 2^23), or 0x7FFFFF so that it always holds).
+// Denormal maxima and anything below the E8M0 range clamp to -127.
+struct ScaleRule {
+  uint32_t mant_thr;
+  uint32_t pow2_down;  // q = 8: M = 2^k gives e = k - 3
+};
+
+__device__ __forceinline__ int block_exponent(float M, ScaleRule r) {
   const uint32_t bits = __float_as_uint(M);
   const int b = static_cast<int>(bits >> 23);
   if (b == 0) return -127;
-  const int e = b - 126 - ((bits & 0x7FFFFFu) <= mant_thr ? 3 : 2);
+  const uint32_t mant = bits & 0x7FFFFFu;
+  const int e = b - 126 - (mant <= r.mant_thr ? 3 : 2) - ((r.pow2_down && mant == 0u) ? 1 : 0);
   return e < -127 ? -127 : e;
 }
 
-uint32_t rule_mantissa_threshold(int rule) {
-  return rule == kRuleOCP ? 0x7FFFFFu : (rule == kRuleTFS ? 0x400000u : 0x680000u);
+ScaleRule make_rule(int rule, double qmax) {
+  ScaleRule r{0x680000u, 0u};
+  if (rule == kRuleOCP) r.mant_thr = 0x7FFFFFu;
+  if (rule == kRuleTFS) r.mant_thr = 0x400000u;
+  if (rule == kRuleCeilQ) {
+    const double t = std::floor((qmax / 4.0 - 1.0) * 8388608.0);  // exact: qmax/4 - 1 has qmax's ulp
+    r.mant_thr = t >= 8388607.0 ? 0x7FFFFFu : static_cast<uint32_t>(t);
+    r.pow2_down = qmax >= 8.0 ? 1u : 0u;
+  }
+  return r;
 }
 
 // 2^-e as binary32; valid for e in [-127, 126], which covers every finite M.
@@ -96,7 +114,7 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
                                                                          uint32_t* __restrict__ codes,
                                                                          uint32_t* __restrict__ scales,
                                                                          int64_t BH, int64_t N, int64_t NT,
-                                                                         uint32_t mant_thr, int rotate) {
+                                                                         ScaleRule rule, int rotate) {
   const int lane = threadIdx.x & 31;
   const int l = lane & 3;
   const int64_t slots_per_head = NT * kTile;
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
       uint32_t word = 0;
       uint32_t sbyte = 127;
       if (m > 0.0f) {
-        const int e = block_exponent(m, mant_thr);
+        const int e = block_exponent(m, rule);
         const float2 inv = make_float2(pow2_neg(e), pow2_neg(e));
         const float2 a = __fmul2_rn(make_float2(c[0], c[1]), inv), b = __fmul2_rn(make_float2(c[2], c[3]), inv);
         const float2 cc = __fmul2_rn(make_float2(c[4], c[5]), inv), d = __fmul2_rn(make_float2(c[6], c[7]), inv);
@@ -214,7 +232,7 @@ constexpr int kVRowWords = kD / 2 + 1;  // bf16x2 words per staged token row (+1
 __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __restrict__ v,
                                                                 uint8_t* __restrict__ codes,
                                                                 uint32_t* __restrict__ scales, int64_t N,
-                                                                int64_t NT, int64_t row_bytes, uint32_t mant_thr) {
+                                                                int64_t NT, int64_t row_bytes, ScaleRule rule) {
   __shared__ uint32_t tile[kTile * kVRowWords];
   const int64_t t = blockIdx.x;
   const int64_t bh = blockIdx.y;
@@ -250,7 +268,7 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
     uint32_t sbyte = 127;
     uint4 packed = make_uint4(0, 0, 0, 0);
     if (m > 0.0f) {
-      const int e = block_exponent(m, mant_thr);
+      const int e = block_exponent(m, rule);
       const float inv = pow2_neg(e);
       uint32_t w4[4];
 #pragma unroll
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
 }  // namespace
 
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
-                                      int rotate, cudaStream_t s) {
+                                      double qmax, int rotate, cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);
   const int64_t groups = ceil_div(BH * NT * kTile, 32 / kQkLanesPerToken);  // one warp-iteration each
   int dev = 0, sms = 0;
@@ -286,18 +304,18 @@ cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void
   rotate_quantize_qk_kernel<<<grid, kQkThreads, 0, s>>>(static_cast<const uint4*>(x),
                                                         static_cast<uint32_t*>(codes),
                                                         static_cast<uint32_t*>(scales), BH, N, NT,
-                                                        rule_mantissa_threshold(rule), rotate);
+                                                        make_rule(rule, qmax), rotate);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,
-                              cudaStream_t s) {
+                              double qmax, cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);
   const int64_t row_bytes = ceil_div(N, kBlock) * kBlock / 2;
   dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
   quantize_v_kernel<<<grid, kVThreads, 0, s>>>(static_cast<const uint4*>(v), static_cast<uint8_t*>(codes),
                                                static_cast<uint32_t*>(scales), N, NT, row_bytes,
-                                               rule_mantissa_threshold(rule));
+                                               make_rule(rule, qmax));
   return cudaGetLastError();
 }
 

@@ -100,14 +100,18 @@ def test_empty_problem_is_a_no_op(lib):
 def test_variant_switches_rejected_on_host(lib):
     """Out-of-range rule / rotate / placement switches of the ablation entry points."""
     big = [ctypes.c_void_p(0x1000000 * (i + 1)) for i in range(8)]
-    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 3, 1, big[1], big[2], None) == 1
+    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 4, 7.25, 1, big[1], big[2], None) == 1
     assert "rule" in _err(lib)
-    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 0, 2, big[1], big[2], None) == 1
+    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 3, 8.5, 1, big[1], big[2], None) == 1
+    assert "qmax" in _err(lib)
+    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 3, 4.0, 1, big[1], big[2], None) == 1
+    assert lib.mxattn_quantize_qk_ex(big[0], 1, 1, 128, 128, 0, 7.25, 2, big[1], big[2], None) == 1
     assert "rotate" in _err(lib)
-    assert lib.mxattn_quantize_v_ex(big[0], 1, 1, 128, 128, -1, big[1], big[2], None) == 1
-    assert lib.mxattn_forward_ex(*big[:6], None, 1, 1, 128, 128, 0, 3, 0, big[6], None) == 1
+    assert lib.mxattn_quantize_v_ex(big[0], 1, 1, 128, 128, -1, 7.25, big[1], big[2], None) == 1
+    assert lib.mxattn_quantize_v_ex(big[0], 1, 1, 128, 128, 3, float("nan"), big[1], big[2], None) == 1
+    assert lib.mxattn_forward_ex(*big[:6], None, 1, 1, 128, 128, 0, 4, 7.25, 0, big[6], None) == 1
     assert "p_rule" in _err(lib)
-    assert lib.mxattn_forward_ex(*big[:6], None, 1, 1, 128, 128, 0, 0, 2, big[6], None) == 1
+    assert lib.mxattn_forward_ex(*big[:6], None, 1, 1, 128, 128, 0, 0, 7.25, 2, big[6], None) == 1
     assert "placement" in _err(lib)
     # empty problems stay no-ops through the variant calls too
-    assert lib.mxattn_quantize_qk_ex(None, 1, 1, 0, 128, 1, 0, None, None, None) == 0
+    assert lib.mxattn_quantize_qk_ex(None, 1, 1, 0, 128, 1, 7.25, 0, None, None, None) == 0

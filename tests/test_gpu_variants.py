@@ -2,8 +2,9 @@
 against the oracle, through the C ABI.
 
 Switches: the block scale rule of every quantizer (UOS, Eq. 13; OCP floor,
-Eq. 11; TFS ceil, Eq. 14), the fixed Hadamard rotation on or off, and where
-l comes from (PNQ, Eq. 47, or direct placement, Eqs. 16-17).
+Eq. 11; TFS ceil, Eq. 14; ceil with a swept Q_max, section 5.5.1), the fixed
+Hadamard rotation on or off, and where l comes from (PNQ, Eq. 47, or direct
+placement, Eqs. 16-17).
   * quantizers: every code and scale byte equals the oracle's;
   * forward: max |O_gpu - O_oracle| <= 2e-3 * RMS(O_oracle) on every row of
     small cases (ragged N, causal and not), for the rows of Table 3 and TFS;
@@ -24,13 +25,16 @@ pytestmark = pytest.mark.gpu
 
 TOL_REL_RMS = 2e-3
 
-# (name, rule of Q/K/V/P~, rotate, placement) -- Table 3 top to bottom, then TFS
+# (name, rule of Q/K/V/P~, rotate, placement, Q_max of the ceil rule) -- Table 3
+# top to bottom, then TFS and two points of the section 5.5.1 Q_max sweep
 CONFIGS = [
-    ("full", 0, True, 0),
-    ("no_uos", 1, True, 0),
-    ("no_uos_no_pnq", 1, True, 1),
-    ("ocp_direct", 1, False, 1),
-    ("tfs_pnq", 2, True, 0),
+    ("full", 0, True, 0, 7.25),
+    ("no_uos", 1, True, 0, 7.25),
+    ("no_uos_no_pnq", 1, True, 1, 7.25),
+    ("ocp_direct", 1, False, 1, 7.25),
+    ("tfs_pnq", 2, True, 0, 7.25),
+    ("ceil_6.8", 3, True, 0, 6.8),
+    ("ceil_8", 3, True, 0, 8.0),
 ]
 
 
@@ -72,36 +76,54 @@ def test_quantize_v_rules(mx, orc, rule):
     assert np.array_equal(gs, os_), f"scale mismatches: {(gs != os_).sum()}"
 
 
-def _run_gpu(mx, q, k, v, rule, rotate, placement, causal):
+@pytest.mark.parametrize("qmax", [6.05, 7.2, 7.3, 8.0])
+def test_quantizers_ceil_rule_any_qmax(mx, orc, qmax):
+    """Section 5.5.1's swept Q_max: codes and scales bit-exact for Q/K (rotated) and V."""
+    q, _, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", H=3, N=1000, seed=4)
     B, H, N, _ = q.shape
-    qc, qs = mx.mxattn_quantize_qk_ex(q, rule=rule, rotate=rotate)
-    kc, ks = mx.mxattn_quantize_qk_ex(k, rule=rule, rotate=rotate)
-    vc, vs = mx.mxattn_quantize_v_ex(v, rule=rule)
-    out = mx.mxattn_forward_ex(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal, p_rule=rule, placement=placement)
+    codes, scales = mx.mxattn_quantize_qk_ex(q, rule=3, qmax=qmax)
+    vcodes, vscales = mx.mxattn_quantize_v_ex(v, rule=3, qmax=qmax)
+    torch.cuda.synchronize()
+    oc, os_ = orc.rotate_quantize_qk(W.as_u16(q).reshape(B * H, N, 128), rule=3, q=qmax)
+    assert np.array_equal(L.qk_codes_logical(codes.cpu().numpy(), B * H, N), oc)
+    assert np.array_equal(L.qk_scales_logical(scales.cpu().numpy(), B * H, N), os_)
+    ovc, ovs = orc.quantize_v(W.as_u16(v).reshape(B * H, N, 128), rule=3, q=qmax)
+    assert np.array_equal(L.v_codes_logical(vcodes.cpu().numpy(), B * H, N), ovc)
+    assert np.array_equal(L.v_scales_logical(vscales.cpu().numpy(), B * H, N), ovs)
+
+
+def _run_gpu(mx, q, k, v, rule, rotate, placement, causal, qmax=7.25):
+    B, H, N, _ = q.shape
+    qc, qs = mx.mxattn_quantize_qk_ex(q, rule=rule, rotate=rotate, qmax=qmax)
+    kc, ks = mx.mxattn_quantize_qk_ex(k, rule=rule, rotate=rotate, qmax=qmax)
+    vc, vs = mx.mxattn_quantize_v_ex(v, rule=rule, qmax=qmax)
+    out = mx.mxattn_forward_ex(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal, p_rule=rule, placement=placement,
+                               p_qmax=qmax)
     mx.mxattn_check()
     return out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
 
 
-def _run_oracle(orc, q, k, v, rule, rotate, placement, causal):
+def _run_oracle(orc, q, k, v, rule, rotate, placement, causal, qmax=7.25):
     B, H, N, _ = q.shape
     qb, kb, vb = (W.as_u16(t).reshape(B * H, N, 128) for t in (q, k, v))
-    qc, qs = orc.rotate_quantize_qk(qb, rule=rule, rotate=rotate)
-    kc, ks = orc.rotate_quantize_qk(kb, rule=rule, rotate=rotate)
-    vc, vs = orc.quantize_v(vb, rule=rule)
+    qc, qs = orc.rotate_quantize_qk(qb, rule=rule, rotate=rotate, q=qmax)
+    kc, ks = orc.rotate_quantize_qk(kb, rule=rule, rotate=rotate, q=qmax)
+    vc, vs = orc.quantize_v(vb, rule=rule, q=qmax)
     rows = np.array([[b, i] for b in range(B * H) for i in range(N)], dtype=np.int64)
-    ref = orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=vb, causal=causal, placement=placement, p_rule=rule)
+    ref = orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=vb, causal=causal, placement=placement, p_rule=rule,
+                      p_q=qmax)
     return ref["out"].reshape(B * H, N, 128)
 
 
-@pytest.mark.parametrize("name,rule,rotate,placement", CONFIGS)
+@pytest.mark.parametrize("name,rule,rotate,placement,qmax", CONFIGS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_forward_variants_all_rows(mx, orc, name, rule, rotate, placement, causal):
+def test_forward_variants_all_rows(mx, orc, name, rule, rotate, placement, qmax, causal):
     if causal:
         q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=700, seed=13)
     else:
         q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=300)
-    g = _run_gpu(mx, q, k, v, rule, rotate, placement, causal)
-    o = _run_oracle(orc, q, k, v, rule, rotate, placement, causal)
+    g = _run_gpu(mx, q, k, v, rule, rotate, placement, causal, qmax)
+    o = _run_oracle(orc, q, k, v, rule, rotate, placement, causal, qmax)
     err = np.abs(g - o).max()
     rms = math.sqrt(np.mean(o ** 2))
     print(f"{name} causal={causal}: max|err| = {err:.3e}, RMS = {rms:.3e}, ratio = {err / rms:.3e}")
