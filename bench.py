@@ -311,6 +311,25 @@ def run_ours(args, w):
         bt = flops / (bms * 1e-3) / 1e12
         bf16_path = {"kernel": "bf16_fwd_kernel (tcgen05 kind::f16)", "ms": bms, "tflops": bt,
                      "frac_of_bf16_peak": bt / bf16, "mxfp4_speedup": bms / fwd_ms}
+        # context: the library BF16 attention on the same tensors (torch SDPA, bf16 output)
+        try:
+            import torch.nn.functional as F
+
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    F.scaled_dot_product_attention(q, k, v, is_causal=w.causal)
+                l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                l0.record(stream)
+                for _ in range(3):
+                    F.scaled_dot_product_attention(q, k, v, is_causal=w.causal)
+                l1.record(stream)
+            torch.cuda.synchronize()
+            lms = l0.elapsed_time(l1) / 3
+            bf16_path["library_sdpa"] = {"api": "torch.nn.functional.scaled_dot_product_attention (bf16)",
+                                         "ms": lms, "tflops": flops / (lms * 1e-3) / 1e12,
+                                         "mxfp4_speedup": lms / fwd_ms}
+        except Exception as ex:  # no fused backend for this GPU / torch build
+            bf16_path["library_sdpa"] = {"unavailable": str(ex)[:200]}
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -385,6 +404,88 @@ ABLATION = [
 ]
 
 
+def _e2m1_lut(device):
+    import torch
+
+    return torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], device=device)
+
+
+def _atom_rows(device):
+    """[128 rows, 4 blocks] -> byte offset in a 512-byte scale atom (include/mxattn.h)."""
+    import torch
+
+    r = torch.arange(128, device=device)[:, None]
+    k = torch.arange(4, device=device)[None, :]
+    return (r % 32) * 16 + (r // 32) * 4 + k
+
+
+def _dequant_qk(codes, scales, BH, N):
+    """Q/K codes [BH][N][64] and scale atoms -> float32 [BH, N, 128]."""
+    import torch
+
+    lut = _e2m1_lut(codes.device)
+    c = codes.view(BH, N, 64).long()
+    vals = torch.stack([lut[c & 15], lut[c >> 4]], -1).view(BH, N, 128)
+    NT = (N + 127) // 128
+    sb = scales.view(BH, NT, 512)[:, :, _atom_rows(codes.device)].reshape(BH, NT * 128, 4)[:, :N]
+    return vals * torch.exp2(sb.float() - 127).repeat_interleave(32, -1)
+
+
+def _dequant_v(codes, scales, BH, N):
+    """V codes [BH][128][Npad/2] and scale atoms -> float32 [BH, N, 128]."""
+    import torch
+
+    lut = _e2m1_lut(codes.device)
+    npad = (N + 31) // 32 * 32
+    c = codes.view(BH, 128, npad // 2).long()
+    vals = torch.stack([lut[c & 15], lut[c >> 4]], -1).view(BH, 128, npad)[:, :, :N]
+    NT = (N + 127) // 128
+    sb = scales.view(BH, NT, 512)[:, :, _atom_rows(codes.device)]          # [BH, NT, 128 ch, 4 blocks]
+    sb = sb.permute(0, 2, 1, 3).reshape(BH, 128, NT * 4).repeat_interleave(32, -1)[:, :, :N]
+    return (vals * torch.exp2(sb.float() - 127)).transpose(1, 2)
+
+
+def run_qmax_sweep(mx, W, names):
+    """Section 5.5.1: for every head and tensor (rotated Q, rotated K, V), the Q_max in
+    6.00 .. 8.00 (steps of 0.05) that minimizes the block quantizer's MSE."""
+    import torch
+
+    grid = [round(6.0 + 0.05 * i, 2) for i in range(41)]
+    H128 = torch.ones(1, 1, device="cuda")
+    while H128.shape[0] < 128:
+        H128 = torch.cat([torch.cat([H128, H128], 1), torch.cat([H128, -H128], 1)], 0)
+    res = {}
+    for wname in names:
+        w = W.WORKLOADS[wname]
+        q, k, v = W.generate(w, device="cuda")
+        B, H, N = w.B, w.H, w.N
+        BH = B * H
+        out = {}
+        for tname, x, rot in (("Q", q, True), ("K", k, True), ("V", v, False)):
+            ref = x.float().reshape(BH, N, 128)
+            if rot:
+                ref = (ref @ H128) * (128 ** -0.5)
+            mse = torch.empty(len(grid), BH, device="cuda")
+            for gi, qm in enumerate(grid):
+                if rot:
+                    c, sc = mx.mxattn_quantize_qk_ex(x, rule=3, qmax=qm)
+                    d = _dequant_qk(c, sc, BH, N)
+                else:
+                    c, sc = mx.mxattn_quantize_v_ex(x, rule=3, qmax=qm)
+                    d = _dequant_v(c, sc, BH, N)
+                mse[gi] = ((d - ref) ** 2).mean(dim=(1, 2))
+                del c, sc, d
+            best = [grid[i] for i in mse.argmin(0).tolist()]
+            hist = {str(g): best.count(g) for g in sorted(set(best))}
+            rel = (mse / mse[grid.index(7.25)]).mean(1).tolist()
+            out[tname] = {"heads": BH, "argmin_counts": hist, "frac_at_7.25": best.count(7.25) / BH,
+                          "mean_mse_rel_to_7.25": {str(g): rel[grid.index(g)] for g in (6.0, 6.5, 7.0, 7.2, 7.25, 7.3, 7.5, 8.0)}}
+        res[wname] = out
+        del q, k, v
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_accuracy(args):
     """Accuracy of the ablation variants and the BF16 path against exact
     softmax attention (Eq. 1, float64 on the host) on sampled rows of every
@@ -445,7 +546,9 @@ def run_accuracy(args):
         table[wname] = {"rows": len(rows), "results": res}
         del q, k, v
         torch.cuda.empty_cache()
-    print(json.dumps({"accuracy": table, "reference": "exact softmax attention (Eq. 1), float64 on the host",
+    sweep = run_qmax_sweep(mx, W, [n for n in ("lognormal_4096", "wan_32760", "hunyuan_118800") if n in names])
+    print(json.dumps({"accuracy": table, "qmax_sweep": sweep,
+                      "reference": "exact softmax attention (Eq. 1), float64 on the host",
                       "data": "synthetic"}), flush=True)
 
 
