@@ -192,6 +192,11 @@ void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, double q
  *   K, V   : N x 128 key / value values (already dequantized)
  *   Vraw   : N x 128 unquantized values, used on the causal diagonal block
  *   i      : the query's token index (causal masking and the diagonal block)
+ * causal: 0 = none; 1 = keys j > i masked and the query's own 32-token V block
+ * taken unquantized from Vraw (the reading that removes the leak the MatX note
+ * describes); 2 = the same mask, with that block re-quantized per channel over
+ * tokens b0..i only (tokens after i left out of the block maximum), using the
+ * P~ rule p_rule / p_q.
  * Options: quant_p (PNQ quantizer on), placement (0 = PNQ: l from P^,
  * 1 = direct: l from P~, Eq. 16-17), p_rule (scale rule for P~), bc (tile).
  * Outputs: o[128], *ell; optional phat[ntiles*bc] (P^ of each tile before any
@@ -220,6 +225,20 @@ static void online_softmax_row(const double* q, const double* K, const double* V
   double* Pt = (double*)malloc(sizeof(double) * bc);
   double* Ph = (double*)malloc(sizeof(double) * bc);
   unsigned char* valid = (unsigned char*)malloc(bc);
+  /* causal == 2: the diagonal V block, re-quantized over tokens b0..i */
+  const int64_t b0 = (i / ORC_BLOCK) * ORC_BLOCK;
+  const int npre = (int)(i - b0 + 1);
+  double* Vd = NULL;
+  if (op->causal == 2) {
+    Vd = (double*)malloc(sizeof(double) * ORC_BLOCK * ORC_D);
+    for (int c = 0; c < ORC_D; c++) {
+      double vals[ORC_BLOCK];
+      uint8_t cb[ORC_BLOCK];
+      for (int t = 0; t < npre; t++) vals[t] = Vraw[(b0 + t) * ORC_D + c];
+      int sb = quantize_block(vals, npre, op->p_rule, op->p_q, cb);
+      for (int t = 0; t < npre; t++) Vd[t * ORC_D + c] = dq(cb[t], (uint8_t)sb);
+    }
+  }
   for (int64_t j = 0; j < ntiles; j++) {
     const int64_t k0 = j * bc;
     /* Eq. 2: S = Q^ K^T / sqrt(d) */
@@ -260,8 +279,8 @@ static void online_softmax_row(const double* q, const double* K, const double* V
     for (int kk = 0; kk < bc; kk++) {
       if (!valid[kk] || Ph[kk] == 0.0) continue;
       int64_t key = k0 + kk;
-      const double* vrow = (op->causal && (key / ORC_BLOCK) == (i / ORC_BLOCK)) ? Vraw + key * ORC_D
-                                                                                 : V + key * ORC_D;
+      const int diag = op->causal && (key / ORC_BLOCK) == (i / ORC_BLOCK);
+      const double* vrow = !diag ? V + key * ORC_D : (op->causal == 2 ? Vd + (key - b0) * ORC_D : Vraw + key * ORC_D);
       for (int c = 0; c < ORC_D; c++) acc[c] += Ph[kk] * vrow[c];
     }
     m = m_new;
@@ -271,6 +290,7 @@ static void online_softmax_row(const double* q, const double* K, const double* V
   /* Eq. 8: O = diag(l)^-1 O */
   for (int c = 0; c < ORC_D; c++) o[c] = acc[c] / ell;
   *ell_out = ell;
+  free(Vd);
   free(S);
   free(Pt);
   free(Ph);

@@ -134,28 +134,29 @@ def _bits(x):
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-def _pipeline(orc, q16, k16, v16, rows, vraw=None):
+def _pipeline(orc, q16, k16, v16, rows, vraw=None, causal=1):
     qc, qs = orc.rotate_quantize_qk(q16)
     kc, ks = orc.rotate_quantize_qk(k16)
     vc, vs = orc.quantize_v(v16)
-    return orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=v16 if vraw is None else vraw, causal=True)
+    return orc.forward(qc, qs, kc, ks, vc, vs, rows, vraw_u16=v16 if vraw is None else vraw, causal=causal)
 
 
-def test_causal_no_future_leakage(orc):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_causal_no_future_leakage(orc, mode):
     rng = np.random.default_rng(15)
     N = 300
     q = rng.standard_normal((1, N, D)) * 2
     k = rng.standard_normal((1, N, D)) * 2
     v = rng.standard_normal((1, N, D))
     rows = np.array([[0, i] for i in [0, 3, 31, 33, 100, 127, 128, 170, 255, 299]])
-    base = _pipeline(orc, _bits(q), _bits(k), _bits(v), rows)["out"]
+    base = _pipeline(orc, _bits(q), _bits(k), _bits(v), rows, causal=mode)["out"]
     for r, (_, i) in enumerate(rows):
         q2, k2, v2 = q.copy(), k.copy(), v.copy()
         fut = slice(i + 1, N)
         q2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
         k2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
         v2[0, fut] = rng.standard_normal((N - i - 1, D)) * 50
-        pert = _pipeline(orc, _bits(q2), _bits(k2), _bits(v2), rows[r:r + 1])["out"]
+        pert = _pipeline(orc, _bits(q2), _bits(k2), _bits(v2), rows[r:r + 1], causal=mode)["out"]
         assert np.array_equal(pert[0], base[r]), f"row {i} changed"
 
 
@@ -182,6 +183,31 @@ def test_causal_leak_without_diagonal_rule(orc):
     v2 = v.copy()
     v2[0, 45, :] = 1000.0  # token 45 > 40, same 32-token block [32, 64)
     assert not np.array_equal(run(v), run(v2))
+
+
+def test_causal_prefix_requantization_reduces_to_the_block_quantizer(orc):
+    """causal = 2 re-quantizes the query's own 32-token V block over tokens b0..i.
+    For the last token of a block (and the last token of a ragged final block)
+    that prefix is the whole block, so the row equals the plain V^ path (the
+    leaky one) bit for bit; for an earlier row it differs."""
+    rng = np.random.default_rng(18)
+    N = 200  # last block 192..199 is ragged
+    Q, K, V = (rng.standard_normal((1, N, D)) for _ in range(3))
+    q16, k16, v16 = _bits(Q), _bits(K), _bits(V)
+    qc, qs = orc.rotate_quantize_qk(q16)
+    kc, ks = orc.rotate_quantize_qk(k16)
+    vc, vs = orc.quantize_v(v16)
+    Qd, Kd, Vd = orc.dequant_qk(qc, qs)[0], orc.dequant_qk(kc, ks)[0], orc.dequant_v(vc, vs)[0]
+    Vraw = v16.astype(np.uint32)[0]
+    Vraw = (Vraw << 16).view(np.float32).astype(np.float64)
+    for i in (31, 63, 127, 199):
+        pre = orc.online_softmax(Qd[i][None], [i], Kd, Vd, Vraw, causal=2)["out"]
+        leaky = orc.online_softmax(Qd[i][None], [i], Kd, Vd, Vd, causal=1)["out"]
+        assert np.array_equal(pre, leaky), i
+    i = 70
+    pre = orc.online_softmax(Qd[i][None], [i], Kd, Vd, Vraw, causal=2)["out"]
+    leaky = orc.online_softmax(Qd[i][None], [i], Kd, Vd, Vd, causal=1)["out"]
+    assert not np.array_equal(pre, leaky)
 
 
 def test_forward_on_codes_matches_real_valued_core(orc):
