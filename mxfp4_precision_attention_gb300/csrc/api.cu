@@ -115,7 +115,7 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   MX_TRY(check_ptr(vc, "v_codes"));
   MX_TRY(check_ptr(vs, "v_scales"));
   MX_TRY(check_ptr(out, "out"));
-  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (causal < 0 || causal > 2) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0, 1 or 2");
   MX_TRY(check_rule(p_rule, p_qmax, "p_rule"));
   if (placement != kPlacePNQ && placement != kPlaceDirect)
     return fail(MXATTN_ERR_INVALID_ARG, "placement must be 0 (PNQ) or 1 (direct)");
@@ -311,6 +311,7 @@ mxattn_status mxattn_forward(const void* q_codes, const void* q_scales, const vo
                              const void* v_codes, const void* v_scales, const void* v_bf16, int64_t B, int64_t H,
                              int64_t N, int64_t D, int causal, float* out, void* stream) {
   t_err[0] = '\0';
+  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
                       nullptr, nullptr, stream);
 }
@@ -322,6 +323,7 @@ mxattn_status mxattn_forward_dump_phat(const void* q_codes, const void* q_scales
   t_err[0] = '\0';
   if (phat_codes == nullptr || phat_scales == nullptr)
     return fail(MXATTN_ERR_INVALID_ARG, "phat_codes and phat_scales are required");
+  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
                       phat_codes, phat_scales, stream);
 }

@@ -35,6 +35,7 @@
 // in the device status word, the waiting warp leaves its loop, and TMEM is
 // released before the CTA returns.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 
@@ -108,6 +109,8 @@ struct Params {
   int p_rule;     // variant kernels only
   int placement;  // variant kernels only
   float p_log2q;  // variant kernels, kRuleCeilQ: log2(Q_max)
+  uint32_t diag_mant_thr;   // causal mode 2: scale rule of the re-quantized diagonal V block
+  uint32_t diag_pow2_down;
   float score_scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -132,6 +135,31 @@ __device__ __forceinline__ float e2m1_decode(uint32_t nib) {
   const float mag = (m < 2u) ? 0.5f * static_cast<float>(m)
                              : (1.0f + 0.5f * static_cast<float>(m & 1u)) * static_cast<float>(1u << ((m >> 1) - 1));
   return (nib & 8u) ? -mag : mag;
+}
+
+// Block exponent of a finite maximum M > 0 under a scale rule given by its
+// mantissa threshold (the quantizers' rule); denormal maxima clamp to -127.
+__device__ __forceinline__ int rule_exponent(float M, uint32_t mant_thr, uint32_t pow2_down) {
+  const uint32_t bits = __float_as_uint(M);
+  const int b = static_cast<int>(bits >> 23);
+  if (b == 0) return -127;
+  const uint32_t mant = bits & 0x7FFFFFu;
+  const int e = b - 126 - (mant <= mant_thr ? 3 : 2) - ((pow2_down && mant == 0u) ? 1 : 0);
+  return e < -127 ? -127 : e;
+}
+
+// 2^e as binary32 for e in [-127, 127] (2^-127 is a denormal)
+__device__ __forceinline__ float pow2i(int e) {
+  return e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// E2M1 round trip of two values (RNE, saturating at 6): the values the codes stand for
+__device__ __forceinline__ float2 e2m1_round2(float y0, float y1) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h)
+      : "f"(y0), "f"(y1));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
 __device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag) {
@@ -629,6 +657,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
+            if (kVariant && p.causal == 2) {
+              // Mode 2: the diagonal V block re-quantized per channel over keys
+              // 0..lane (this row's prefix). Lane l reads key l's row; an
+              // inclusive prefix-max scan over the lanes gives each row its
+              // per-channel block maxima. Keys after the row have P^ = 0.
+              float mx[32];
+              {
+                const uint4* mine = slot + lane * 4;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) {
+                  const uint4 u = mine[q4];
+                  const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int t2 = 0; t2 < 4; t2++) {
+                    mx[8 * q4 + 2 * t2] = fabsf(__uint_as_float(uu[t2] << 16));
+                    mx[8 * q4 + 2 * t2 + 1] = fabsf(__uint_as_float(uu[t2] & 0xFFFF0000u));
+                  }
+                }
+              }
+#pragma unroll
+              for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                  const float other = __shfl_up_sync(0xffffffffu, mx[i], d);
+                  if (lane >= d) mx[i] = fmaxf(mx[i], other);
+                }
+              }
+              float inv[32], t[32];
+#pragma unroll
+              for (int i = 0; i < 32; i++) {
+                const int e = mx[i] > 0.0f ? rule_exponent(mx[i], p.diag_mant_thr, p.diag_pow2_down) : 0;
+                inv[i] = pow2i(-e);
+                t[i] = 0.0f;
+              }
+#pragma unroll 1
+              for (int kk = 0; kk < 4; kk++) {
+                const uint32_t wk = kk == 0 ? diag_words[0] : (kk == 1 ? diag_words[1] : (kk == 2 ? diag_words[2] : diag_words[3]));
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                  const float pk = e2m1_decode((wk >> (4 * k)) & 0xFu) * dsc;
+                  const uint4* vr = slot + (8 * kk + k) * 4;
+#pragma unroll
+                  for (int q4 = 0; q4 < 4; q4++) {
+                    const uint4 u = vr[q4];
+                    const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int t2 = 0; t2 < 4; t2++) {
+                      const int c0 = 8 * q4 + 2 * t2;
+                      const float2 y = __fmul2_rn(make_float2(__uint_as_float(uu[t2] << 16), __uint_as_float(uu[t2] & 0xFFFF0000u)),
+                                                  make_float2(inv[c0], inv[c0 + 1]));
+                      const float2 dq = e2m1_round2(y.x, y.y);
+                      const float2 r = __ffma2_rn(make_float2(pk, pk), dq, make_float2(t[c0], t[c0 + 1]));
+                      t[c0] = r.x;
+                      t[c0 + 1] = r.y;
+                    }
+                  }
+                }
+              }
+              // 2^e = 1 / 2^-e exactly (IEEE reciprocal of a power of two)
+#pragma unroll
+              for (int i = 0; i < 32; i++) acc[i] = fmaf(__frcp_rn(inv[i]), t[i], acc[i]);
+            } else {
             // masked keys (beyond the row or beyond N) have P^ = 0; their staged
             // rows are finite (zeros past N)
 #pragma unroll 1
@@ -649,6 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                 }
               }
+            }
             }
             if (qrow < N) {
               float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
@@ -707,6 +798,7 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.p_rule = a.p_rule;
   p.placement = a.placement;
   p.p_log2q = static_cast<float>(std::log2(a.p_qmax));
+  rule_threshold(a.p_rule, a.p_qmax, &p.diag_mant_thr, &p.diag_pow2_down);
   p.score_scale_log2 = kLog2e / 11.313708498984761f;  // log2(e) / sqrt(128)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -724,7 +816,7 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   }
   dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
   const bool dump = a.phat_codes != nullptr;
-  const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ;
+  const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ || a.causal == 2;
   if (variant && dump) return cudaErrorNotSupported;  // the P^ dump covers UOS + PNQ only
   if (variant) {
     if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);

@@ -20,6 +20,12 @@ enum : uint32_t { kDebugNeverArriveS = 1u };
 enum : int { kRuleUOS = 0, kRuleOCP = 1, kRuleTFS = 2, kRuleCeilQ = 3 };
 enum : int { kPlacePNQ = 0, kPlaceDirect = 1 };
 
+// Mantissa-field threshold of a block scale rule (see quantize.cu): the
+// exponent of a block maximum M = 1.f * 2^(b-127) is (b-126) - 3 if the
+// mantissa field is <= mant_thr, else (b-126) - 2, and one lower for an exact
+// power of two when pow2_down is set.
+void rule_threshold(int rule, double qmax, uint32_t* mant_thr, uint32_t* pow2_down);
+
 // qmax is used by kRuleCeilQ only (a value in (4, 8]).
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       double qmax, int rotate, cudaStream_t s);
@@ -35,7 +41,7 @@ struct Mxfp4FwdArgs {
   const void* v_scales;
   const void* v_bf16;  // causal diagonal blocks
   int64_t BH, N;
-  int causal;
+  int causal;  // 0, 1, or 2: diagonal V block re-quantized over the prefix (variant kernel)
   float* out;
   uint8_t* phat_codes;   // optional diagnostic dump, [BH][N][ceil(N/128)*64]
   uint8_t* phat_scales;  // optional diagnostic dump, [BH][N][ceil(N/128)*4]

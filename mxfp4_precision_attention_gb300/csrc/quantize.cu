@@ -292,6 +292,12 @@ __global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __re
 
 }  // namespace
 
+void rule_threshold(int rule, double qmax, uint32_t* mant_thr, uint32_t* pow2_down) {
+  const ScaleRule r = make_rule(rule, qmax);
+  *mant_thr = r.mant_thr;
+  *pow2_down = r.pow2_down;
+}
+
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       double qmax, int rotate, cudaStream_t s) {
   const int64_t NT = ceil_div(N, kTile);

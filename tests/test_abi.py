@@ -113,5 +113,9 @@ def test_variant_switches_rejected_on_host(lib):
     assert "p_rule" in _err(lib)
     assert lib.mxattn_forward_ex(*big[:6], None, 1, 1, 128, 128, 0, 0, 7.25, 2, big[6], None) == 1
     assert "placement" in _err(lib)
+    # causal = 2 (prefix re-quantized diagonal block) exists only in mxattn_forward_ex
+    assert lib.mxattn_forward(*big[:6], big[7], 1, 1, 128, 128, 2, big[6], None) == 1
+    assert "causal" in _err(lib)
+    assert lib.mxattn_forward_ex(*big[:6], big[7], 1, 1, 128, 128, 3, 0, 7.25, 0, big[6], None) == 1
     # empty problems stay no-ops through the variant calls too
     assert lib.mxattn_quantize_qk_ex(None, 1, 1, 0, 128, 1, 7.25, 0, None, None, None) == 0

@@ -156,3 +156,34 @@ def test_rowsum_control_v_ones(mx, orc, causal):
     print(f"direct placement, V == 1: max |O - 1| gpu {dev_gpu:.3e}, oracle {dev_ora:.3e}")
     assert dev_gpu > 1e-3 and dev_ora > 1e-3
 
+
+
+@pytest.mark.parametrize("rule,placement", [(0, 0), (1, 1)])
+def test_causal_prefix_mode_all_rows(mx, orc, rule, placement):
+    """causal = 2: the query's own V block re-quantized over its prefix (the other
+    reading of the MatX note's fix), against the oracle on every row."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=700, seed=23)
+    B, H, N, _ = q.shape
+    g = _run_gpu(mx, q, k, v, rule, True, placement, 2)
+    o = _run_oracle(orc, q, k, v, rule, True, placement, 2)
+    err = np.abs(g - o).max()
+    rms = math.sqrt(np.mean(o ** 2))
+    print(f"prefix causal rule={rule} placement={placement}: max|err| = {err:.3e}, ratio = {err / rms:.3e}")
+    assert err <= TOL_REL_RMS * rms
+    # and it is not the bf16-diagonal reading
+    assert not np.array_equal(g, _run_gpu(mx, q, k, v, rule, True, placement, 1))
+
+
+def test_causal_prefix_mode_no_future_leakage(mx):
+    """Perturbing every token after i leaves GPU row i bit-identical under causal = 2."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=1, N=300, seed=29)
+    base = _run_gpu(mx, q, k, v, 0, True, 0, 2)
+    g = torch.Generator(device="cpu").manual_seed(31)
+    for i in (0, 5, 31, 40, 127, 128, 200, 299):
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
+        n = 300 - i - 1
+        if n > 0:
+            for t in (q2, k2, v2):
+                t[0, 0, i + 1:] = (torch.randn(n, 128, generator=g) * 40).to(t.dtype).to(t.device)
+        pert = _run_gpu(mx, q2, k2, v2, 0, True, 0, 2)
+        assert np.array_equal(pert[0, i], base[0, i]), f"row {i} changed"
