@@ -486,6 +486,67 @@ def run_qmax_sweep(mx, W, names):
     return res
 
 
+def run_rowsum_diagnostic(mx, W, names, rows_per_workload=256):
+    """Section 5.5.2 on synthetic heads: materialize P = softmax(S) for sampled rows
+    (exact S from the bf16 Q, K), round it to bf16, quantize it in 32-key MXFP4
+    blocks with the library's quantizer (rotation off), and report the mean row sum
+    of the quantized P, the row-sum error split into zeroing, saturation, downward
+    and upward rounding, and the row sums by attention entropy."""
+    import torch
+
+    out = {}
+    for wname in names:
+        w = W.WORKLOADS[wname]
+        q, k, _ = W.generate(w, device="cuda")
+        B, H, N = w.B, w.H, w.N
+        g = torch.Generator().manual_seed(4321)
+        heads = torch.randperm(B * H, generator=g)[: min(4, B * H)].tolist()
+        per = max(1, rows_per_workload // len(heads))
+        qf, kf = q.reshape(B * H, N, 128), k.reshape(B * H, N, 128)
+        Ps = []
+        for h in heads:
+            ii = torch.randint(0, N, (per,), generator=g).cuda()
+            s = (qf[h, ii].double() @ kf[h].double().T) / 128 ** 0.5
+            if w.causal:
+                s = s.masked_fill(torch.arange(N, device="cuda")[None, :] > ii[:, None], -float("inf"))
+            Ps.append(torch.softmax(s, 1))
+        P = torch.cat(Ps)                                          # [R, N] float64
+        R = P.shape[0]
+        npad = (N + 127) // 128 * 128
+        Pb = torch.zeros((R, npad), dtype=torch.bfloat16, device="cuda")
+        Pb[:, :N] = P.to(torch.bfloat16)
+        Pr = Pb.double()                                           # what the quantizer sees
+        x = Pb.reshape(1, 1, R * npad // 128, 128)
+        ent = -(P * torch.log(P.clamp_min(1e-300))).sum(1)
+        res = {}
+        for rname, rule in (("UOS", 0), ("OCP", 1)):
+            c, sc = mx.mxattn_quantize_qk_ex(x, rule=rule, rotate=False)
+            Qp = _dequant_qk(c, sc, 1, R * npad // 128).reshape(R, npad).double()
+            d = Qp - Pr
+            blk = Pr.reshape(R, npad // 32, 32).amax(2, keepdim=True)
+            e = torch.ceil(torch.log2(blk / 7.25)) if rule == 0 else torch.floor(torch.log2(blk)) - 2
+            sat = (Pr.reshape(R, npad // 32, 32) / torch.exp2(e) > 6).reshape(R, npad) & (Pr > 0)
+            zero = (Qp == 0) & (Pr > 0)
+            down = (d < 0) & ~zero & ~sat
+            up = d > 0
+            rs = Qp.sum(1)
+            parts = {name: (d * m).sum(1).mean().item() for name, m in
+                     (("zeroing", zero), ("saturation", sat), ("rounding_down", down), ("rounding_up", up))}
+            bins = {}
+            for lo, hi in ((0, 1), (1, 3), (3, 5), (5, 1e9)):
+                m = (ent >= lo) & (ent < hi)
+                if m.any():
+                    bins[f"entropy [{lo}, {hi if hi < 1e9 else 'inf'})"] = {
+                        "rows": int(m.sum()), "mean_rowsum": rs[m].mean().item(),
+                        "frac_below_1": (rs[m] < 1).double().mean().item()}
+            res[rname] = {"mean_rowsum": rs.mean().item(), "min_rowsum": rs.min().item(),
+                          "max_rowsum": rs.max().item(), "error_parts": parts, "by_entropy": bins}
+        out[wname] = {"rows": R, "mean_entropy": ent.mean().item(), "results": res}
+        del q, k
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_accuracy(args):
     """Accuracy of the ablation variants and the BF16 path against exact
     softmax attention (Eq. 1, float64 on the host) on sampled rows of every
@@ -547,7 +608,8 @@ def run_accuracy(args):
         del q, k, v
         torch.cuda.empty_cache()
     sweep = run_qmax_sweep(mx, W, [n for n in ("lognormal_4096", "wan_32760", "hunyuan_118800") if n in names])
-    print(json.dumps({"accuracy": table, "qmax_sweep": sweep,
+    rowsum = run_rowsum_diagnostic(mx, W, names)
+    print(json.dumps({"accuracy": table, "qmax_sweep": sweep, "rowsum_diagnostic": rowsum,
                       "reference": "exact softmax attention (Eq. 1), float64 on the host",
                       "data": "synthetic"}), flush=True)
 
