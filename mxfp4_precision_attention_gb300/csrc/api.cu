@@ -415,8 +415,22 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
   if (hp == nullptr) return cuda_fail(e, "host copy streams");
   std::lock_guard<std::mutex> lock(hp->mu);
   const int64_t BH = B * H;
-  const int64_t nchunks = BH < kHostChunks ? BH : kHostChunks;
-  const int64_t per = ceil_div(BH, nchunks);
+  // Chunk boundaries: the first and the last chunk hold one head, so the
+  // kernels start after a short copy and the final copy out is short; the
+  // heads in between are spread evenly over the remaining chunks.
+  int64_t bounds[kHostChunks + 1];
+  int64_t nchunks = 0;
+  {
+    const int64_t edge = BH >= 4 ? 1 : 0;
+    const int64_t mid_heads = BH - 2 * edge;
+    const int64_t mid_chunks = mid_heads < kHostChunks - 2 * edge ? mid_heads : kHostChunks - 2 * edge;
+    const int64_t per = ceil_div(mid_heads, mid_chunks);
+    bounds[0] = 0;
+    if (edge) bounds[++nchunks] = 1;
+    for (int64_t h = edge + per; h < BH - edge; h += per) bounds[++nchunks] = h;
+    if (edge) bounds[++nchunks] = BH - 1;
+    bounds[++nchunks] = BH;
+  }
   const int64_t NT = ceil_div(N, kTile), npad_half = ceil_div(N, kBlock) * kBlock / 2;
   const size_t xh = static_cast<size_t>(N) * kD * 2, oh = static_cast<size_t>(N) * kD * 4;
   const size_t qch = static_cast<size_t>(N) * 64, sfh = static_cast<size_t>(NT) * kSfAtomBytes,
@@ -429,8 +443,7 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
   const char* hv = static_cast<const char*>(v_host);
   char* ho = reinterpret_cast<char*>(out_host);
   for (int64_t c = 0; c < nchunks; c++) {
-    const int64_t h0 = c * per, hn = (BH - h0) < per ? (BH - h0) : per;
-    if (hn <= 0) break;
+    const int64_t h0 = bounds[c], hn = bounds[c + 1] - bounds[c];
     const size_t xo = h0 * xh, xn = hn * xh;
     if ((e = cudaMemcpyAsync(q + xo, hq + xo, xn, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) return cuda_fail(e, "copy q");
     if ((e = cudaMemcpyAsync(k + xo, hk + xo, xn, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) return cuda_fail(e, "copy k");
