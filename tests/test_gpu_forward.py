@@ -249,9 +249,9 @@ def test_host_entry_point_matches_device_path(mx):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_host_entry_point_pipelined_chunks(mx, causal):
-    """21 heads run as 11 chunks of two heads (the last holds one) whose copies
-    overlap the kernels; two calls in a row (the internal streams and events
-    are reused) give the device path's output bit for bit."""
+    """21 heads run as 16 chunks (one head in the first and in the last) whose
+    copies overlap the kernels; two calls in a row (the internal streams and
+    events are reused) give the device path's output bit for bit."""
     q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=3, H=7, N=300, seed=17)
     dev = _gpu_mx(mx, q, k, v, causal=causal).cpu()
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
