@@ -225,69 +225,82 @@ __global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const ui
 }
 
 // ----------------------------------------------------------------- (b)
-// One CTA per (head, 128-token tile); thread c owns channel c.
-constexpr int kVThreads = 128;
-constexpr int kVRowWords = kD / 2 + 1;  // bf16x2 words per staged token row (+1 pad)
+// One CTA per (head, 128-token tile), eight warps. Warp w takes token block
+// w/2 (32 tokens) of channel half w%2 (64 channels); lane l owns channels
+// c0 = 64*(w%2) + 2l and c0 + 1, i.e. the l-th bf16x2 word of the half row.
+// Each load instruction reads 128 contiguous bytes of one token row; a lane
+// ends up with its two channels' whole 32-token block, so block maxima and
+// codes need no exchange between threads. Only the scale atom is assembled in
+// shared memory.
+constexpr int kVThreads = 256;
 
-__global__ void __launch_bounds__(kVThreads) quantize_v_kernel(const uint4* __restrict__ v,
-                                                                uint8_t* __restrict__ codes,
-                                                                uint32_t* __restrict__ scales, int64_t N,
-                                                                int64_t NT, int64_t row_bytes, ScaleRule rule) {
-  __shared__ uint32_t tile[kTile * kVRowWords];
+__global__ void __launch_bounds__(kVThreads, 3) quantize_v_kernel(const uint32_t* __restrict__ v,
+                                                                   uint8_t* __restrict__ codes,
+                                                                   uint32_t* __restrict__ scales, int64_t N,
+                                                                   int64_t NT, int64_t row_bytes, ScaleRule rule) {
+  __shared__ uint32_t atom[kSfAtomBytes / 4];
   const int64_t t = blockIdx.x;
   const int64_t bh = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int64_t n0 = t * kTile;
-  // stage 128 tokens x 128 channels (16-byte coalesced loads; tokens >= N read as 0)
-#pragma unroll 4
-  for (int i = tid; i < kTile * 16; i += kVThreads) {
-    const int row = i / 16, q = i % 16;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (n0 + row < N) val = ld_nc_v4(v + (bh * N + n0 + row) * 16 + q);
-    uint32_t* dst = tile + row * kVRowWords + q * 4;
-    dst[0] = val.x;
-    dst[1] = val.y;
-    dst[2] = val.z;
-    dst[3] = val.w;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int half = warp & 1, kb = warp >> 1;
+  const int c0 = 64 * half + 2 * lane;
+  const int64_t tok0 = t * kTile + kb * kBlock;
+  const uint32_t* src = v + (bh * N + tok0) * (kD / 2) + 32 * half + lane;
+  uint32_t w[kBlock];
+#pragma unroll
+  for (int i = 0; i < kBlock; i++) w[i] = tok0 + i < N ? __ldg(src + i * (kD / 2)) : 0u;
+  // |.| maxima of both channels at once: bf16 max is exact
+  uint32_t mw = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int i = 1; i < kBlock; i++) {
+    const uint32_t a = w[i] & 0x7FFF7FFFu;
+    asm("max.bf16x2 %0, %0, %1;" : "+r"(mw) : "r"(a));
+  }
+  float lo_m, hi_m;
+  bf16x2_to_f32(mw, lo_m, hi_m);
+  const float m2[2] = {lo_m, hi_m};
+  uint32_t sb[2];
+  float inv[2];
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const bool nz = m2[h] > 0.0f;
+    const int e = nz ? block_exponent(m2[h], rule) : 0;
+    sb[h] = nz ? static_cast<uint32_t>(e + 127) : 127u;
+    inv[h] = nz ? pow2_neg(e) : 0.0f;
+  }
+  uint32_t cw[2][4];
+  const float2 inv2 = make_float2(inv[0], inv[1]);
+#pragma unroll
+  for (int g = 0; g < 4; g++) {
+    float q0[8], q1[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      float lo, hi;
+      bf16x2_to_f32(w[8 * g + i], lo, hi);
+      const float2 q = __fmul2_rn(make_float2(lo, hi), inv2);
+      q0[i] = q.x;
+      q1[i] = q.y;
+    }
+    cw[0][g] = pack_e2m1x8(q0[0], q0[1], q0[2], q0[3], q0[4], q0[5], q0[6], q0[7]);
+    cw[1][g] = pack_e2m1x8(q1[0], q1[1], q1[2], q1[3], q1[4], q1[5], q1[6], q1[7]);
+  }
+  if (tok0 < N) {  // block holds at least one real token; it lies inside Npad
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+      *reinterpret_cast<uint4*>(codes + (bh * kD + c0 + h) * row_bytes + tok0 / 2) =
+          make_uint4(cw[h][0], cw[h][1], cw[h][2], cw[h][3]);
+  }
+  // scale byte of row c, block kb -> (c%32)*16 + (c/32)*4 + kb
+  uint8_t* ab = reinterpret_cast<uint8_t*>(atom);
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const int c = c0 + h;
+    ab[(c % 32) * 16 + (c / 32) * 4 + kb] = static_cast<uint8_t>(sb[h]);
   }
   __syncthreads();
-  const int c = tid;
-  const int word = c >> 1;
-  const bool hi_half = (c & 1) != 0;
-  uint32_t sw = 0;
-#pragma unroll
-  for (int kb = 0; kb < kTile / kBlock; kb++) {
-    float val[kBlock];
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kBlock; i++) {
-      const uint32_t w = tile[(kb * kBlock + i) * kVRowWords + word];
-      val[i] = hi_half ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
-      m = fmaxf(m, fabsf(val[i]));
-    }
-    uint32_t sbyte = 127;
-    uint4 packed = make_uint4(0, 0, 0, 0);
-    if (m > 0.0f) {
-      const int e = block_exponent(m, rule);
-      const float inv = pow2_neg(e);
-      uint32_t w4[4];
-#pragma unroll
-      for (int g = 0; g < 4; g++) {
-        w4[g] = pack_e2m1x8(__fmul_rn(val[8 * g + 0], inv), __fmul_rn(val[8 * g + 1], inv),
-                            __fmul_rn(val[8 * g + 2], inv), __fmul_rn(val[8 * g + 3], inv),
-                            __fmul_rn(val[8 * g + 4], inv), __fmul_rn(val[8 * g + 5], inv),
-                            __fmul_rn(val[8 * g + 6], inv), __fmul_rn(val[8 * g + 7], inv));
-      }
-      packed = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      sbyte = static_cast<uint32_t>(e + 127);
-    }
-    sw |= sbyte << (8 * kb);
-    const int64_t tok0 = n0 + kb * kBlock;
-    if (tok0 < N) {  // block holds at least one real token; it lies inside Npad
-      *reinterpret_cast<uint4*>(codes + (bh * kD + c) * row_bytes + tok0 / 2) = packed;
-    }
-  }
-  scales[(bh * NT + t) * (kSfAtomBytes / 4) + (c % 32) * 4 + (c / 32)] = sw;
+  if (threadIdx.x < kSfAtomBytes / 16)
+    reinterpret_cast<uint4*>(scales + (bh * NT + t) * (kSfAtomBytes / 4))[threadIdx.x] =
+        reinterpret_cast<const uint4*>(atom)[threadIdx.x];
 }
 
 }  // namespace
@@ -319,7 +332,7 @@ cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes,
   const int64_t NT = ceil_div(N, kTile);
   const int64_t row_bytes = ceil_div(N, kBlock) * kBlock / 2;
   dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
-  quantize_v_kernel<<<grid, kVThreads, 0, s>>>(static_cast<const uint4*>(v), static_cast<uint8_t*>(codes),
+  quantize_v_kernel<<<grid, kVThreads, 0, s>>>(static_cast<const uint32_t*>(v), static_cast<uint8_t*>(codes),
                                                static_cast<uint32_t*>(scales), N, NT, row_bytes,
                                                make_rule(rule, qmax));
   return cudaGetLastError();
