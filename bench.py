@@ -1,8 +1,8 @@
 """Benchmark of the MXAttention MXFP4 forward hot path on GB300.
 
 One step = the whole hot path over one batch of synthetic input:
-mxattn_rotate_quantize_qk(Q), mxattn_rotate_quantize_qk(K), mxattn_quantize_v(V),
-mxattn_forward -- four kernel launches on one stream, inputs resident in HBM.
+mxattn_quantize_qkv (Q and K rotated and quantized, V quantized: one launch)
+and mxattn_forward -- two kernel launches on one stream, inputs resident in HBM.
 
 Default workload: the video-DiT shaped configuration B=1, H=40, N=32760
 (21x30x52 latent tokens), d=128, non-causal, seeded synthetic bf16 Q, K, V
@@ -247,13 +247,10 @@ def run_ours(args, w):
     def step(i=None):
         e = ev[i] if i is not None else None
         if e: e[0].record(stream)
-        mx.mxattn_rotate_quantize_qk(q, qc, qs, stream=stream)
-        mx.mxattn_rotate_quantize_qk(k, kc, ks, stream=stream)
+        mx.mxattn_quantize_qkv(q, k, v, out=(qc, qs, kc, ks, vc, vs), stream=stream)
         if e: e[1].record(stream)
-        mx.mxattn_quantize_v(v, vc, vs, stream=stream)
-        if e: e[2].record(stream)
         mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=w.causal, out=out, stream=stream)
-        if e: e[3].record(stream)
+        if e: e[2].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -284,15 +281,28 @@ def run_ours(args, w):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
         dist.barrier()
-    qk_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_events))
-    v_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_events))
-    fwd_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(n_events))
+    qkv_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_events))
+    fwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_events))
     flops = w.flops
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
     fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
     e = B * H * N * 128
-    qk_bytes = 2 * (e * 2 + mx.qk_layout_sizes(B, H, N)[0] + mx.qk_layout_sizes(B, H, N)[1])
-    v_bytes = e * 2 + vcn + vsn
+    qkv_bytes = 2 * (e * 2 + qcn + qsn) + e * 2 + vcn + vsn
+
+    # the three single-tensor quantizer calls, for comparison with the one launch (not part of the step)
+    single = None
+    with torch.cuda.stream(stream):
+        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for rep in range(4):
+            if rep == 3: s_ev[0].record(stream)
+            mx.mxattn_rotate_quantize_qk(q, qc, qs, stream=stream)
+            mx.mxattn_rotate_quantize_qk(k, kc, ks, stream=stream)
+            if rep == 3: s_ev[1].record(stream)
+            mx.mxattn_quantize_v(v, vc, vs, stream=stream)
+            if rep == 3: s_ev[2].record(stream)
+    torch.cuda.synchronize()
+    mx.mxattn_check(stream)
+    single = {"rotate_quantize_qk_x2_ms": s_ev[0].elapsed_time(s_ev[1]), "quantize_v_ms": s_ev[1].elapsed_time(s_ev[2])}
 
     # the BF16 comparison path on the same inputs (not part of the step)
     bf16_path = None
@@ -379,10 +389,12 @@ def run_ours(args, w):
                          "traffic_note": "DRAM bytes per launch, scaled by B*H from an 8-head ncu capture of the same kernel source",
                          "kernel": "mxfp4_fwd_kernel",
                          "peak_source": f"{peak_src} bf16 {bf16:.1f} TF/s x nominal fp4/bf16 ratio {FP4_OVER_BF16_NOMINAL:g}"},
-            "breakdown_ms": {"rotate_quantize_qk_x2": qk_ms, "quantize_v": v_ms, "forward": fwd_ms},
-            "quantizer_gbs": {"qk": qk_bytes / (qk_ms * 1e-3) / 1e9, "v": v_bytes / (v_ms * 1e-3) / 1e9,
-                              "hbm_peak": hbm},
-            "gpu_launches": 4 * args.steps,
+            "breakdown_ms": {"quantize_qkv": qkv_ms, "forward": fwd_ms},
+            "quantizer": {"kernel": "quantize_tiles_kernel (one launch for Q, K, V)",
+                          "algorithmic_bytes": qkv_bytes, "gbs": qkv_bytes / (qkv_ms * 1e-3) / 1e9,
+                          "frac_of_hbm": qkv_bytes / (qkv_ms * 1e-3) / 1e9 / hbm, "hbm_peak": hbm,
+                          "single_calls": single},
+            "gpu_launches": 2 * args.steps,
             "bf16_path": bf16_path,
             "clocks": clk,
             "e2e": e2e,

@@ -89,6 +89,21 @@ MXATTN_API mxattn_status mxattn_rotate_quantize_qk(const void* x, int64_t B, int
 MXATTN_API mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
                                 void* scales, void* stream);
 
+/* Q, K and V quantized in one launch ("MXAttention" section 5.6: the rotation
+ * and the block quantization act on Q/K tiles locally, so they belong in the
+ * Q/K preprocessing stage). Writes exactly what mxattn_rotate_quantize_qk(q),
+ * mxattn_rotate_quantize_qk(k) and mxattn_quantize_v(v) write, byte for byte,
+ * from one persistent kernel in which the 128-token tiles of the three
+ * tensors interleave.
+ *   q, k, v                            : bf16 [B, H, N, 128] (device, read only)
+ *   q_codes/q_scales, k_codes/k_scales : as for mxattn_rotate_quantize_qk
+ *   v_codes/v_scales                   : as for mxattn_quantize_v
+ * No output may overlap an input or another output (inputs may alias each
+ * other). Errors as for the single-tensor calls. */
+MXATTN_API mxattn_status mxattn_quantize_qkv(const void* q, const void* k, const void* v, int64_t B, int64_t H,
+                                             int64_t N, int64_t D, void* q_codes, void* q_scales, void* k_codes,
+                                             void* k_scales, void* v_codes, void* v_scales, void* stream);
+
 /* Algorithm 2 (section 4.3), the attention loop, on quantized operands: for every query row, key
  * tiles of Bc = 128 in increasing order; S = Q^K^T/sqrt(d) and P^V^ on
  * tcgen05 block-scaled MXFP4 tensor cores; running max m, rescale
@@ -170,8 +185,7 @@ MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);
 /* The whole forward from host memory: copies q/k/v (bf16 [B,H,N,128], host;
  * page-locked memory gives full copy bandwidth and lets the copies overlap
  * the kernels) into `workspace` (device, >= mxattn_workspace_bytes, 256-byte
- * aligned), runs mxattn_rotate_quantize_qk (Q and K), mxattn_quantize_v and
- * mxattn_forward, copies the fp32 result to out_host, and synchronizes
+ * aligned), runs mxattn_quantize_qkv and mxattn_forward, copies the fp32 result to out_host, and synchronizes
  * `stream` before returning, so out_host is ready on MXATTN_OK.
  * The B*H heads run as up to 16 chunks: each chunk's copy in, kernels and
  * copy out are ordered by events, with the copies on two internal streams

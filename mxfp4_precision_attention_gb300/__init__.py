@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MxattnError", "load", "mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward",
+    "MxattnError", "load", "mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_quantize_qkv", "mxattn_forward",
     "mxattn_forward_dump_phat", "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_workspace_bytes",
     "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
     "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes",
@@ -56,6 +56,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             getattr(lib, name).restype = SZ
         lib.mxattn_rotate_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P]
         lib.mxattn_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P]
+        lib.mxattn_quantize_qkv.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, P, P, P]
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
@@ -133,6 +134,22 @@ def mxattn_quantize_v(v: torch.Tensor, codes: torch.Tensor | None = None, scales
     scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
     _raise(load().mxattn_quantize_v(_ptr(v), B, H, N, Dx, _ptr(codes), _ptr(scales), _stream(stream)))
     return codes, scales
+
+
+def mxattn_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out=None, stream=None):
+    """Q and K rotated and quantized, V quantized, in one launch. Returns
+    (q_codes, q_scales, k_codes, k_scales, v_codes, v_scales), the same bytes
+    the three single-tensor calls write; `out` may supply those six buffers."""
+    B, H, N, Dx = _shape(q)
+    if _shape(k) != (B, H, N, Dx) or _shape(v) != (B, H, N, Dx):
+        raise ValueError("q, k and v must have the same shape")
+    if out is None:
+        nc, ns = qk_layout_sizes(B, H, N)
+        vc, vs = v_layout_sizes(B, H, N)
+        out = tuple(torch.empty(n, dtype=torch.uint8, device=q.device) for n in (nc, ns, nc, ns, vc, vs))
+    _raise(load().mxattn_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, *(_ptr(t) for t in out),
+                                      _stream(stream)))
+    return tuple(out)
 
 
 def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,

@@ -101,6 +101,14 @@ mxattn_status check_rule(int rule, double qmax, const char* what) {
   return MXATTN_OK;
 }
 
+// The quantizers launch through a TMA tensor map and report expired waits in
+// the device status word.
+mxattn_status check_quantizer_runtime() {
+  if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
+  return MXATTN_OK;
+}
+
 mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                            const void* vs, const void* vb, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                            float* out, uint8_t* pc, uint8_t* ps, void* stream, int p_rule = kRuleUOS,
@@ -278,6 +286,7 @@ mxattn_status mxattn_quantize_qk_ex(const void* x, int64_t B, int64_t H, int64_t
   const Range rx = rng(x, bf16_bytes(B, H, N)), rc = rng(codes, qk_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
   if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs))
     return fail(MXATTN_ERR_INVALID_ARG, "x, codes and scales must not overlap");
+  MX_TRY(check_quantizer_runtime());
   cudaError_t e =
       launch_rotate_quantize_qk(x, B * H, N, codes, scales, rule, qmax, rotate, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_qk launch");
@@ -302,8 +311,45 @@ mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t 
   const Range rv = rng(v, bf16_bytes(B, H, N)), rc = rng(codes, v_codes(B, H, N)), rs = rng(scales, sf_bytes(B, H, N));
   if (overlap(rv, rc) || overlap(rv, rs) || overlap(rc, rs))
     return fail(MXATTN_ERR_INVALID_ARG, "v, codes and scales must not overlap");
+  MX_TRY(check_quantizer_runtime());
   cudaError_t e = launch_quantize_v(v, B * H, N, codes, scales, rule, qmax, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_v launch");
+  return MXATTN_OK;
+}
+
+mxattn_status mxattn_quantize_qkv(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
+                                  int64_t D, void* q_codes, void* q_scales, void* k_codes, void* k_scales,
+                                  void* v_codes, void* v_scales, void* stream) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(q, "q"));
+  MX_TRY(check_ptr(k, "k"));
+  MX_TRY(check_ptr(v, "v"));
+  MX_TRY(check_ptr(q_codes, "q_codes"));
+  MX_TRY(check_ptr(q_scales, "q_scales"));
+  MX_TRY(check_ptr(k_codes, "k_codes"));
+  MX_TRY(check_ptr(k_scales, "k_scales"));
+  MX_TRY(check_ptr(v_codes, "v_codes"));
+  MX_TRY(check_ptr(v_scales, "v_scales"));
+  const size_t xb = bf16_bytes(B, H, N);
+  const Range in[3] = {rng(q, xb), rng(k, xb), rng(v, xb)};
+  const Range outs[6] = {rng(q_codes, qk_codes(B, H, N)), rng(q_scales, sf_bytes(B, H, N)),
+                         rng(k_codes, qk_codes(B, H, N)), rng(k_scales, sf_bytes(B, H, N)),
+                         rng(v_codes, mxattn_v_codes_bytes(B, H, N)), rng(v_scales, sf_bytes(B, H, N))};
+  for (int i = 0; i < 6; i++) {
+    for (int j = 0; j < 3; j++)
+      if (overlap(outs[i], in[j])) return fail(MXATTN_ERR_INVALID_ARG, "an output overlaps an input");
+    for (int j = i + 1; j < 6; j++)
+      if (overlap(outs[i], outs[j])) return fail(MXATTN_ERR_INVALID_ARG, "two outputs overlap");
+  }
+  MX_TRY(check_quantizer_runtime());
+  const QuantizeJob jobs[3] = {{q, q_codes, q_scales, kRuleUOS, 7.25, 0, 1},
+                               {k, k_codes, k_scales, kRuleUOS, 7.25, 0, 1},
+                               {v, v_codes, v_scales, kRuleUOS, 7.25, 1, 0}};
+  cudaError_t e = launch_quantize(jobs, 3, B * H, N, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize_qkv launch");
   return MXATTN_OK;
 }
 
@@ -454,9 +500,7 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
     if ((e = cudaStreamWaitEvent(cs, hp->ev_in[c], 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
     uint8_t *cq = qc + h0 * qch, *ck = kc + h0 * qch, *cv = vc + h0 * vch;
     uint8_t *sq = qs + h0 * sfh, *sk = ks + h0 * sfh, *sv = vs + h0 * sfh;
-    MX_TRY(mxattn_rotate_quantize_qk(q + xo, 1, hn, N, D, cq, sq, cstream));
-    MX_TRY(mxattn_rotate_quantize_qk(k + xo, 1, hn, N, D, ck, sk, cstream));
-    MX_TRY(mxattn_quantize_v(v + xo, 1, hn, N, D, cv, sv, cstream));
+    MX_TRY(mxattn_quantize_qkv(q + xo, k + xo, v + xo, 1, hn, N, D, cq, sq, ck, sk, cv, sv, cstream));
     float* co = reinterpret_cast<float*>(reinterpret_cast<char*>(out) + h0 * oh);
     MX_TRY(mxattn_forward(cq, sq, ck, sk, cv, sv, v + xo, 1, hn, N, D, causal, co, cstream));
     if ((e = cudaEventRecord(hp->ev_out[c], cs)) != cudaSuccess) return cuda_fail(e, "event record");

@@ -26,7 +26,20 @@ enum : int { kPlacePNQ = 0, kPlaceDirect = 1 };
 // power of two when pow2_down is set.
 void rule_threshold(int rule, double qmax, uint32_t* mant_thr, uint32_t* pow2_down);
 
-// qmax is used by kRuleCeilQ only (a value in (4, 8]).
+// One tensor of a quantizer launch: bf16 [BH][N][128] in, codes and scales
+// out (layouts in quantize.cu). qmax is used by kRuleCeilQ only (a value in
+// (4, 8]); rotate applies to Q/K jobs only.
+struct QuantizeJob {
+  const void* x;
+  void* codes;
+  void* scales;
+  int rule;
+  double qmax;
+  int is_v;
+  int rotate;
+};
+// Up to three jobs of the same B*H and N in one launch (their tiles interleave).
+cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int64_t N, cudaStream_t s);
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       double qmax, int rotate, cudaStream_t s);
 cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,

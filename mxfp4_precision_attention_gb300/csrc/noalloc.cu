@@ -99,11 +99,7 @@ extern "C" mxattn_status mxattn_attention_noalloc(const void* q, const void* k, 
   uint8_t* vs = vc + up256(mxattn_v_codes_bytes(B, H, N));
   // Every byte the forward reads is rewritten by the quantizers below, so
   // nothing in the scratch needs clearing between calls.
-  mxattn_status st = mxattn_rotate_quantize_qk(q, B, H, N, D, qc, qs, stream);
-  if (st != MXATTN_OK) return st;
-  st = mxattn_rotate_quantize_qk(k, B, H, N, D, kc, ks, stream);
-  if (st != MXATTN_OK) return st;
-  st = mxattn_quantize_v(v, B, H, N, D, vc, vs, stream);
+  const mxattn_status st = mxattn_quantize_qkv(q, k, v, B, H, N, D, qc, qs, kc, ks, vc, vs, stream);
   if (st != MXATTN_OK) return st;
   return mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, D, causal, out, stream);
 }

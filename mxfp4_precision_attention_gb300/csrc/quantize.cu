@@ -2,6 +2,9 @@
 // and quantization steps of Algorithm 2 in section 4.3, with the UOS block
 // quantizer of Algorithm 1).
 //
+// Both run in one kernel (quantize_tiles_kernel below), one launch per call;
+// mxattn_quantize_qkv runs all three tensors of a forward in one launch.
+//
 //  (a) rotate_quantize_qk: per token, Hadamard-rotate the 128 channels
 //      (binary32 butterflies h = 1,2,...,64, then x 2^-3.5 rounded to binary32)
 //      and quantize each 32-channel block to E2M1 with the UOS scale
@@ -20,6 +23,7 @@
 //               (rows = tokens for Q/K, channels for V; blocks = channel blocks
 //               for Q/K, token blocks for V). Rows or blocks past N hold 127.
 //   scale byte = e + 127 (E8M0); an all-zero block gets 127 and zero codes.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -75,23 +79,6 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// ----------------------------------------------------------------- (a)
-// Four lanes per token. Lane l holds the 8-channel chunks c = 4k + l
-// (k = 0..3), i.e. z[8k + i] is channel 8(4k + l) + i. In this layout the
-// butterflies h = 1, 2, 4 (inside a chunk) and h = 32, 64 (chunk k ^ 1,
-// k ^ 2) stay in the lane; only h = 8 and h = 16 pair lanes l ^ 1 and l ^ 2.
-// Each load instruction reads whole 64-byte segments of 8 token rows.
-constexpr int kQkThreads = 256;
-constexpr int kQkLanesPerToken = 4;
-
 // One butterfly on a register pair: (a, b) -> (a + b, a - b) in binary32.
 __device__ __forceinline__ void bfly(float& a, float& b) {
   const float s = __fadd_rn(a, b), d = __fsub_rn(a, b);
@@ -110,197 +97,276 @@ __device__ __forceinline__ void bfly2(float& a0, float& a1, float& b0, float& b1
   b1 = d.y;
 }
 
-__global__ void __launch_bounds__(kQkThreads) rotate_quantize_qk_kernel(const uint4* __restrict__ x,
-                                                                         uint32_t* __restrict__ codes,
-                                                                         uint32_t* __restrict__ scales,
-                                                                         int64_t BH, int64_t N, int64_t NT,
-                                                                         ScaleRule rule, int rotate) {
-  const int lane = threadIdx.x & 31;
-  const int l = lane & 3;
-  const int64_t slots_per_head = NT * kTile;
-  const int64_t total_slots = BH * slots_per_head;
-  constexpr int kTokPerWarp = 32 / kQkLanesPerToken;
-  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kQkThreads / 32);
-  // h = 8, 16: the lane holding the lower channel of the pair adds, the other subtracts
-  const float sgn8 = (l & 1) ? -1.0f : 1.0f, sgn16 = (l & 2) ? -1.0f : 1.0f;
-  for (int64_t grp = static_cast<int64_t>(blockIdx.x) * (kQkThreads / 32) + threadIdx.x / 32;
-       grp * kTokPerWarp < total_slots; grp += warps_total) {
-    const int64_t slot = grp * kTokPerWarp + lane / kQkLanesPerToken;
-    const bool in_range = slot < total_slots;
-    const int64_t bh = in_range ? slot / slots_per_head : 0;
-    const int64_t n = in_range ? slot - bh * slots_per_head : 0;
-    const bool real = in_range && n < N;
-    float z[32];
-    if (real) {
-      const uint4* row = x + (bh * N + n) * 16;
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// max |v[i]| over 32 values
+__device__ __forceinline__ float absmax32(const float* v) {
+  float a[11];
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const uint4 raw = ld_nc_v4(row + 4 * k + l);
-        bf16x2_to_f32(raw.x, z[8 * k + 0], z[8 * k + 1]);
-        bf16x2_to_f32(raw.y, z[8 * k + 2], z[8 * k + 3]);
-        bf16x2_to_f32(raw.z, z[8 * k + 4], z[8 * k + 5]);
-        bf16x2_to_f32(raw.w, z[8 * k + 6], z[8 * k + 7]);
-      }
-    } else {
+  for (int i = 0; i < 10; i++) a[i] = max3f(fabsf(v[3 * i]), fabsf(v[3 * i + 1]), fabsf(v[3 * i + 2]));
+  a[10] = fmaxf(fabsf(v[30]), fabsf(v[31]));
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]), b2 = max3f(a[6], a[7], a[8]);
+  return max3f(max3f(b0, b1, b2), a[9], a[10]);
+}
+
+__device__ __forceinline__ void record_error(int* status, int code, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicCAS(status, 0, code);
+}
+
+// ----------------------------------------------------------------- kernel
+// One persistent kernel serves every quantizer call. A work unit is one
+// 128-token tile of one head of one tensor: 128 rows of 256 bytes, brought
+// into shared memory by two TMA loads (channels 0-63 and 64-127; 128 bytes
+// per row each, 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ (r % 8)), into a ring of kQStages buffers. All four warps quantize;
+// thread 0 also refills the ring: once every warp has read unit i-1 into
+// registers, it loads unit i-1+kQStages into that buffer. Units of up to
+// three tensors (Q, K, V of one call) interleave, so the rotation's ALU work
+// and the V tiles' light work share the SMs.
+//
+//  (a) Q/K tile: one thread per token, its 128 channels in registers in
+//      natural order. The h = 1 butterflies pair the halves of a register
+//      pair (scalar adds); h = 2 ... 64 pair register pair (i, i+1) with
+//      (i+h, i+h+1) (packed f32x2 adds). Same binary32 operations in the same
+//      stage order as the plain definition.
+//  (b) V tile: warp w takes token block w (32 tokens); lane l owns channels
+//      2l, 2l+1, 64+2l, 65+2l (word l of each half row), so every block
+//      maximum and code is formed inside the thread.
+// Two CTAs of four warps per SM: a Q/K thread holds a token's 128 channels
+// (192 registers, no spills), and the register file is split per SMSP
+// (16K each), so two 4-warp CTAs (two warps per SMSP) is the most that fits;
+// three 32 KB stages each keep six tiles in flight per SM.
+constexpr int kQStages = 3;
+constexpr int kQMinBlocks = 2;
+constexpr int kQThreads = 128;  // four warps; thread 0 also issues the loads
+constexpr int kQConsumers = 128;
+constexpr uint32_t kQHalfBytes = kTile * 128;        // one TMA box: 128 rows x 64 channels
+constexpr uint32_t kQStageBytes = 2 * kQHalfBytes;   // 32 KB
+constexpr uint32_t kQSmemBytes = kQStages * kQStageBytes + 2 * kQStages * 8 + 16 + 1024;
+
+struct QTensor {
+  uint8_t* codes;
+  uint32_t* scales;
+  ScaleRule rule;
+  int is_v;    // 0: Q/K (per-token channel blocks), 1: V (per-channel token blocks)
+  int rotate;  // Q/K only
+};
+struct QParams {
+  QTensor t[3];
+  int ntensors;
+  int64_t BH, N, NT, row_bytes;  // row_bytes: V codes per channel row (Npad/2)
+  int64_t units;                 // ntensors * BH * NT
+  int* status;
+};
+
+__device__ __forceinline__ void quantize_qk_tile(const uint8_t* tile, int r, int64_t bh, int64_t t, const QParams& p,
+                                                 const QTensor& T, uint32_t empty_bar) {
+  float z[kD];
 #pragma unroll
-      for (int i = 0; i < 32; i++) z[i] = 0.0f;
+  for (int c = 0; c < kD / 8; c++) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kQHalfBytes + r * 128 +
+                                                      (((c & 7) ^ (r & 7)) << 4));
+    bf16x2_to_f32(raw.x, z[8 * c + 0], z[8 * c + 1]);
+    bf16x2_to_f32(raw.y, z[8 * c + 2], z[8 * c + 3]);
+    bf16x2_to_f32(raw.z, z[8 * c + 4], z[8 * c + 5]);
+    bf16x2_to_f32(raw.w, z[8 * c + 6], z[8 * c + 7]);
+  }
+  // the tile is in registers: hand the stage back to the producer
+  __syncwarp();
+  if ((r & 31) == 0) mbar_arrive(empty_bar);
+  if (T.rotate) {
+#pragma unroll
+    for (int i = 0; i < kD; i += 2) bfly(z[i], z[i + 1]);  // h = 1
+#pragma unroll
+    for (int h = 2; h < kD; h *= 2) {
+#pragma unroll
+      for (int i = 0; i < kD; i += 2)
+        if ((i & h) == 0) bfly2(z[i], z[i + 1], z[i + h], z[i + h + 1]);
     }
-    if (rotate) {
+    const float2 rs = make_float2(kRotScale, kRotScale);
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        float* c = z + 8 * k;
-        // h = 1
-        bfly(c[0], c[1]);
-        bfly(c[2], c[3]);
-        bfly(c[4], c[5]);
-        bfly(c[6], c[7]);
-        // h = 2
-        bfly2(c[0], c[1], c[2], c[3]);
-        bfly2(c[4], c[5], c[6], c[7]);
-        // h = 4
-        bfly2(c[0], c[1], c[4], c[5]);
-        bfly2(c[2], c[3], c[6], c[7]);
-      }
-      // h = 8 (lane ^ 1), h = 16 (lane ^ 2): new = own * sign + partner
-#pragma unroll
-      for (int st = 0; st < 2; st++) {
-        const int mask = st ? 2 : 1;
-        const float sg = st ? sgn16 : sgn8;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = __shfl_xor_sync(0xffffffffu, z[i], mask);
-          const float p1 = __shfl_xor_sync(0xffffffffu, z[i + 1], mask);
-          const float2 r = __ffma2_rn(make_float2(z[i], z[i + 1]), make_float2(sg, sg), make_float2(p0, p1));
-          z[i] = r.x;
-          z[i + 1] = r.y;
-        }
-      }
-      // h = 32 (chunk k ^ 1), h = 64 (chunk k ^ 2)
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        bfly2(z[i], z[i + 1], z[8 + i], z[9 + i]);
-        bfly2(z[16 + i], z[17 + i], z[24 + i], z[25 + i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        bfly2(z[i], z[i + 1], z[16 + i], z[17 + i]);
-        bfly2(z[8 + i], z[9 + i], z[24 + i], z[25 + i]);
-      }
-      const float2 rs = make_float2(kRotScale, kRotScale);
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 r = __fmul2_rn(make_float2(z[i], z[i + 1]), rs);
-        z[i] = r.x;
-        z[i + 1] = r.y;
-      }
+    for (int i = 0; i < kD; i += 2) {
+      const float2 v = __fmul2_rn(make_float2(z[i], z[i + 1]), rs);
+      z[i] = v.x;
+      z[i + 1] = v.y;
     }
-    // block k = channels 32k .. 32k+31 = chunk k of the token's four lanes
-    uint32_t sw = 0;
+  }
+  const int64_t n = t * kTile + r;
+  const bool real = n < p.N;
+  uint4* crow = reinterpret_cast<uint4*>(T.codes) + (bh * p.N + n) * (kD / 32);
+  uint32_t sw = 0;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      const float* c = z + 8 * k;
-      float m = fmaxf(fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3]))),
-                      fmaxf(fmaxf(fabsf(c[4]), fabsf(c[5])), fmaxf(fabsf(c[6]), fabsf(c[7]))));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      uint32_t word = 0;
-      uint32_t sbyte = 127;
-      if (m > 0.0f) {
-        const int e = block_exponent(m, rule);
-        const float2 inv = make_float2(pow2_neg(e), pow2_neg(e));
-        const float2 a = __fmul2_rn(make_float2(c[0], c[1]), inv), b = __fmul2_rn(make_float2(c[2], c[3]), inv);
-        const float2 cc = __fmul2_rn(make_float2(c[4], c[5]), inv), d = __fmul2_rn(make_float2(c[6], c[7]), inv);
-        word = pack_e2m1x8(a.x, a.y, b.x, b.y, cc.x, cc.y, d.x, d.y);
-        sbyte = static_cast<uint32_t>(e + 127);
+  for (int k = 0; k < kD / kBlock; k++) {
+    const float* c = z + kBlock * k;
+    const float m = absmax32(c);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    uint32_t sbyte = 127;
+    if (m > 0.0f) {
+      const int e = block_exponent(m, T.rule);
+      const float2 inv = make_float2(pow2_neg(e), pow2_neg(e));
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        const float* cg = c + 8 * g;
+        const float2 a = __fmul2_rn(make_float2(cg[0], cg[1]), inv), b = __fmul2_rn(make_float2(cg[2], cg[3]), inv);
+        const float2 cc = __fmul2_rn(make_float2(cg[4], cg[5]), inv), d = __fmul2_rn(make_float2(cg[6], cg[7]), inv);
+        w[g] = pack_e2m1x8(a.x, a.y, b.x, b.y, cc.x, cc.y, d.x, d.y);
       }
-      if (real) codes[(bh * N + n) * 16 + 4 * k + l] = word;
-      sw |= sbyte << (8 * k);
+      sbyte = static_cast<uint32_t>(e + 127);
     }
-    if (in_range && l == 0) {
-      const int64_t t = n / kTile;
-      const int r = static_cast<int>(n - t * kTile);
-      scales[(bh * NT + t) * (kSfAtomBytes / 4) + (r % 32) * 4 + (r / 32)] = sw;
+    if (real) crow[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    sw |= sbyte << (8 * k);
+  }
+  // padding rows (n >= N) read zeros and store byte 127 in every block
+  T.scales[(bh * p.NT + t) * (kSfAtomBytes / 4) + (r % 32) * 4 + (r / 32)] = sw;
+}
+
+__device__ __forceinline__ void quantize_v_tile(const uint8_t* tile, int kb, int lane, int64_t bh, int64_t t,
+                                                const QParams& p, const QTensor& T, uint32_t empty_bar) {
+  uint32_t w[2][kBlock];
+#pragma unroll
+  for (int i = 0; i < kBlock; i++) {
+    const int row = kb * kBlock + i;
+    const int off = row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) + ((lane & 3) << 2);
+    w[0][i] = *reinterpret_cast<const uint32_t*>(tile + off);
+    w[1][i] = *reinterpret_cast<const uint32_t*>(tile + kQHalfBytes + off);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+  const int64_t tok0 = t * kTile + kb * kBlock;
+  uint8_t* sbytes = reinterpret_cast<uint8_t*>(T.scales + (bh * p.NT + t) * (kSfAtomBytes / 4));
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    // |.| maxima of both channels of the word at once: bf16 max is exact
+    uint32_t mw = w[h][0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 1; i < kBlock; i++) {
+      const uint32_t a = w[h][i] & 0x7FFF7FFFu;
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(mw) : "r"(a));
+    }
+    float m2[2];
+    bf16x2_to_f32(mw, m2[0], m2[1]);
+    uint32_t sb[2];
+    float inv[2];
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      const bool nz = m2[q] > 0.0f;
+      const int e = nz ? block_exponent(m2[q], T.rule) : 0;
+      sb[q] = nz ? static_cast<uint32_t>(e + 127) : 127u;
+      inv[q] = nz ? pow2_neg(e) : 0.0f;
+    }
+    uint32_t cw[2][4];
+    const float2 inv2 = make_float2(inv[0], inv[1]);
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+      float q0[8], q1[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        float lo, hi;
+        bf16x2_to_f32(w[h][8 * g + i], lo, hi);
+        const float2 q = __fmul2_rn(make_float2(lo, hi), inv2);
+        q0[i] = q.x;
+        q1[i] = q.y;
+      }
+      cw[0][g] = pack_e2m1x8(q0[0], q0[1], q0[2], q0[3], q0[4], q0[5], q0[6], q0[7]);
+      cw[1][g] = pack_e2m1x8(q1[0], q1[1], q1[2], q1[3], q1[4], q1[5], q1[6], q1[7]);
+    }
+    const int c0 = 64 * h + 2 * lane;
+    if (tok0 < p.N) {  // block holds at least one real token; it lies inside Npad
+#pragma unroll
+      for (int q = 0; q < 2; q++)
+        *reinterpret_cast<uint4*>(T.codes + (bh * kD + c0 + q) * p.row_bytes + tok0 / 2) =
+            make_uint4(cw[q][0], cw[q][1], cw[q][2], cw[q][3]);
+    }
+    // scale byte of row c, block kb -> (c%32)*16 + (c/32)*4 + kb
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+      const int c = c0 + q;
+      sbytes[(c % 32) * 16 + (c / 32) * 4 + kb] = static_cast<uint8_t>(sb[q]);
     }
   }
 }
 
-// ----------------------------------------------------------------- (b)
-// One CTA per (head, 128-token tile), eight warps. Warp w takes token block
-// w/2 (32 tokens) of channel half w%2 (64 channels); lane l owns channels
-// c0 = 64*(w%2) + 2l and c0 + 1, i.e. the l-th bf16x2 word of the half row.
-// Each load instruction reads 128 contiguous bytes of one token row; a lane
-// ends up with its two channels' whole 32-token block, so block maxima and
-// codes need no exchange between threads. Only the scale atom is assembled in
-// shared memory.
-constexpr int kVThreads = 256;
-
-__global__ void __launch_bounds__(kVThreads, 3) quantize_v_kernel(const uint32_t* __restrict__ v,
-                                                                   uint8_t* __restrict__ codes,
-                                                                   uint32_t* __restrict__ scales, int64_t N,
-                                                                   int64_t NT, int64_t row_bytes, ScaleRule rule) {
-  __shared__ uint32_t atom[kSfAtomBytes / 4];
-  const int64_t t = blockIdx.x;
-  const int64_t bh = blockIdx.y;
+__global__ void __launch_bounds__(kQThreads, kQMinBlocks)
+    quantize_tiles_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+                          const __grid_constant__ CUtensorMap m2, const __grid_constant__ QParams p) {
+  extern __shared__ __align__(1024) uint8_t qsmem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQStages * kQStageBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kQStages);
+  const uint32_t sb = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kQStages + s]); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int half = warp & 1, kb = warp >> 1;
-  const int c0 = 64 * half + 2 * lane;
-  const int64_t tok0 = t * kTile + kb * kBlock;
-  const uint32_t* src = v + (bh * N + tok0) * (kD / 2) + 32 * half + lane;
-  uint32_t w[kBlock];
-#pragma unroll
-  for (int i = 0; i < kBlock; i++) w[i] = tok0 + i < N ? __ldg(src + i * (kD / 2)) : 0u;
-  // |.| maxima of both channels at once: bf16 max is exact
-  uint32_t mw = w[0] & 0x7FFF7FFFu;
-#pragma unroll
-  for (int i = 1; i < kBlock; i++) {
-    const uint32_t a = w[i] & 0x7FFF7FFFu;
-    asm("max.bf16x2 %0, %0, %1;" : "+r"(mw) : "r"(a));
-  }
-  float lo_m, hi_m;
-  bf16x2_to_f32(mw, lo_m, hi_m);
-  const float m2[2] = {lo_m, hi_m};
-  uint32_t sb[2];
-  float inv[2];
-#pragma unroll
-  for (int h = 0; h < 2; h++) {
-    const bool nz = m2[h] > 0.0f;
-    const int e = nz ? block_exponent(m2[h], rule) : 0;
-    sb[h] = nz ? static_cast<uint32_t>(e + 127) : 127u;
-    inv[h] = nz ? pow2_neg(e) : 0.0f;
-  }
-  uint32_t cw[2][4];
-  const float2 inv2 = make_float2(inv[0], inv[1]);
-#pragma unroll
-  for (int g = 0; g < 4; g++) {
-    float q0[8], q1[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      float lo, hi;
-      bf16x2_to_f32(w[8 * g + i], lo, hi);
-      const float2 q = __fmul2_rn(make_float2(lo, hi), inv2);
-      q0[i] = q.x;
-      q1[i] = q.y;
+  const bool leader = threadIdx.x == 0;
+  const int nt = p.ntensors;
+  // unit g (global) -> tensor g % nt, tile g / nt = (head, 128-token tile)
+  auto issue = [&](uint32_t j) {  // local unit j of this CTA into stage j % kQStages
+    const int64_t g = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+    const int s = j % kQStages;
+    const int ti = static_cast<int>(g % nt);
+    const int64_t tile = g / nt;
+    const int bh = static_cast<int>(tile / p.NT);
+    const int t = static_cast<int>(tile - static_cast<int64_t>(bh) * p.NT);
+    const CUtensorMap* m = ti == 0 ? &m0 : (ti == 1 ? &m1 : &m2);
+    mbar_arrive_expect_tx(full(s), kQStageBytes);
+    tma_load_3d(sb + s * kQStageBytes, m, full(s), 0, t * kTile, bh);
+    tma_load_3d(sb + s * kQStageBytes + kQHalfBytes, m, full(s), 64, t * kTile, bh);
+  };
+  const uint32_t nunits =
+      p.units > blockIdx.x ? static_cast<uint32_t>((p.units - blockIdx.x + gridDim.x - 1) / gridDim.x) : 0u;
+  uint32_t issued = 0;
+  if (leader) {
+    *abort_flag = 0;
+    for (int s = 0; s < kQStages; s++) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kQConsumers / 32);
     }
-    cw[0][g] = pack_e2m1x8(q0[0], q0[1], q0[2], q0[3], q0[4], q0[5], q0[6], q0[7]);
-    cw[1][g] = pack_e2m1x8(q1[0], q1[1], q1[2], q1[3], q1[4], q1[5], q1[6], q1[7]);
-  }
-  if (tok0 < N) {  // block holds at least one real token; it lies inside Npad
-#pragma unroll
-    for (int h = 0; h < 2; h++)
-      *reinterpret_cast<uint4*>(codes + (bh * kD + c0 + h) * row_bytes + tok0 / 2) =
-          make_uint4(cw[h][0], cw[h][1], cw[h][2], cw[h][3]);
-  }
-  // scale byte of row c, block kb -> (c%32)*16 + (c/32)*4 + kb
-  uint8_t* ab = reinterpret_cast<uint8_t*>(atom);
-#pragma unroll
-  for (int h = 0; h < 2; h++) {
-    const int c = c0 + h;
-    ab[(c % 32) * 16 + (c / 32) * 4 + kb] = static_cast<uint8_t>(sb[h]);
+    fence_mbar_init();
+    prefetch_tmap(&m0);
+    if (nt > 1) prefetch_tmap(&m1);
+    if (nt > 2) prefetch_tmap(&m2);
+    for (; issued < nunits && issued < static_cast<uint32_t>(kQStages); issued++) issue(issued);
   }
   __syncthreads();
-  if (threadIdx.x < kSfAtomBytes / 16)
-    reinterpret_cast<uint4*>(scales + (bh * NT + t) * (kSfAtomBytes / 4))[threadIdx.x] =
-        reinterpret_cast<const uint4*>(atom)[threadIdx.x];
+  for (uint32_t i = 0; i < nunits; i++) {
+    // the leader refills the stage that unit i-1 used with unit i-1+kQStages,
+    // once all four warps have read unit i-1 into registers
+    if (leader && i >= 1 && issued < nunits) {
+      const uint32_t prev = i - 1;
+      if (!mbar_wait(empty(prev % kQStages), (prev / kQStages) & 1, abort_flag)) {
+        record_error(p.status, 4, const_cast<int*>(abort_flag));
+      } else {
+        issue(issued);
+        issued++;
+      }
+    }
+    const int s = i % kQStages;
+    if (!mbar_wait(full(s), (i / kQStages) & 1, abort_flag)) {
+      record_error(p.status, 4, const_cast<int*>(abort_flag));
+      break;
+    }
+    const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+    const int ti = static_cast<int>(g % nt);
+    const int64_t tile = g / nt;
+    const int64_t bh = tile / p.NT;
+    const int64_t t = tile - bh * p.NT;
+    // a copy picked by value: a run-time index into the parameter array would go through local memory
+    const QTensor T = ti == 0 ? p.t[0] : (ti == 1 ? p.t[1] : p.t[2]);
+    const uint8_t* st = smem + s * kQStageBytes;
+    if (T.is_v)
+      quantize_v_tile(st, warp, lane, bh, t, p, T, empty(s));
+    else
+      quantize_qk_tile(st, threadIdx.x, bh, t, p, T, empty(s));
+  }
+  // after an abort, every copy the leader issued must land before the CTA exits
+  if (leader && *abort_flag) {
+    for (uint32_t j = 0; j < issued; j++) mbar_wait(full(j % kQStages), (j / kQStages) & 1, abort_flag);
+  }
 }
 
 }  // namespace
@@ -311,31 +377,64 @@ void rule_threshold(int rule, double qmax, uint32_t* mant_thr, uint32_t* pow2_do
   *pow2_down = r.pow2_down;
 }
 
+cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int64_t N, cudaStream_t s) {
+  if (njobs < 1 || njobs > 3) return cudaErrorInvalidValue;
+  const int64_t NT = ceil_div(N, kTile);
+  QParams p{};
+  alignas(64) CUtensorMap maps[3];
+  for (int j = 0; j < njobs; j++) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(N) * kD * 2};
+    const uint32_t box[3] = {64, kTile, 1};
+    if (!encode_tensor_map(&maps[j], 1, 3, const_cast<void*>(jobs[j].x), dims, strides, box, 128))
+      return cudaErrorInvalidValue;
+    p.t[j].codes = static_cast<uint8_t*>(jobs[j].codes);
+    p.t[j].scales = static_cast<uint32_t*>(jobs[j].scales);
+    p.t[j].rule = make_rule(jobs[j].rule, jobs[j].qmax);
+    p.t[j].is_v = jobs[j].is_v;
+    p.t[j].rotate = jobs[j].rotate;
+  }
+  for (int j = njobs; j < 3; j++) maps[j] = maps[0];
+  p.ntensors = njobs;
+  p.BH = BH;
+  p.N = N;
+  p.NT = NT;
+  p.row_bytes = ceil_div(N, kBlock) * kBlock / 2;
+  p.units = njobs * BH * NT;
+  p.status = device_status_ptr();
+  if (p.status == nullptr) return cudaErrorInvalidDevice;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int sms[64] = {0};
+  static bool attr_set[64] = {false};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(quantize_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  // persistent: as many CTAs per SM as registers and shared memory allow
+  const int64_t want = kQMinBlocks * static_cast<int64_t>(sms[dev]);
+  const int grid = static_cast<int>(p.units < want ? p.units : want);
+  quantize_tiles_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(maps[0], maps[1], maps[2], p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       double qmax, int rotate, cudaStream_t s) {
-  const int64_t NT = ceil_div(N, kTile);
-  const int64_t groups = ceil_div(BH * NT * kTile, 32 / kQkLanesPerToken);  // one warp-iteration each
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = ceil_div(groups, kQkThreads / 32);
-  const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
-  rotate_quantize_qk_kernel<<<grid, kQkThreads, 0, s>>>(static_cast<const uint4*>(x),
-                                                        static_cast<uint32_t*>(codes),
-                                                        static_cast<uint32_t*>(scales), BH, N, NT,
-                                                        make_rule(rule, qmax), rotate);
-  return cudaGetLastError();
+  const QuantizeJob j{x, codes, scales, rule, qmax, 0, rotate};
+  return launch_quantize(&j, 1, BH, N, s);
 }
 
 cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                               double qmax, cudaStream_t s) {
-  const int64_t NT = ceil_div(N, kTile);
-  const int64_t row_bytes = ceil_div(N, kBlock) * kBlock / 2;
-  dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
-  quantize_v_kernel<<<grid, kVThreads, 0, s>>>(static_cast<const uint32_t*>(v), static_cast<uint8_t*>(codes),
-                                               static_cast<uint32_t*>(scales), N, NT, row_bytes,
-                                               make_rule(rule, qmax));
-  return cudaGetLastError();
+  const QuantizeJob j{v, codes, scales, rule, qmax, 1, 0};
+  return launch_quantize(&j, 1, BH, N, s);
 }
 
 }  // namespace mxattn

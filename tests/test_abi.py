@@ -76,6 +76,14 @@ def test_invalid_arguments_rejected_on_host(lib):
     # overlapping outputs
     a = ctypes.c_void_p(0x100000)
     assert lib.mxattn_rotate_quantize_qk(a, 1, 1, 128, 128, ctypes.c_void_p(0x100000 + 4096), fake, None) == 1
+    # single-launch Q/K/V quantizer: misaligned, overlapping outputs, output over an input
+    big9 = [ctypes.c_void_p(0x1000000 * (i + 1)) for i in range(9)]
+    assert lib.mxattn_quantize_qkv(*big9[:3], 1, 1, 128, 128, *big9[3:8], odd, None) == 1
+    assert "aligned" in _err(lib)
+    assert lib.mxattn_quantize_qkv(*big9[:3], 1, 1, 128, 128, *big9[3:8], big9[7], None) == 1
+    assert "overlap" in _err(lib)
+    assert lib.mxattn_quantize_qkv(*big9[:3], 1, 1, 128, 128, big9[1], *big9[4:9], None) == 1
+    assert lib.mxattn_quantize_qkv(*big9[:3], 1, 1, 128, 64, *big9[3:9], None) == 2
     # causal needs the bf16 V
     big = [ctypes.c_void_p(0x1000000 * (i + 1)) for i in range(8)]
     assert lib.mxattn_forward(*big[:6], None, 1, 1, 128, 128, 1, big[6], None) == 1
@@ -95,6 +103,7 @@ def test_empty_problem_is_a_no_op(lib):
     assert lib.mxattn_quantize_v(None, 0, 4, 100, 128, None, None, None) == 0
     assert lib.mxattn_forward(None, None, None, None, None, None, None, 1, 1, 0, 128, 1, None, None) == 0
     assert lib.mxattn_forward_bf16(None, None, None, 1, 0, 10, 128, 0, None, None) == 0
+    assert lib.mxattn_quantize_qkv(None, None, None, 1, 1, 0, 128, None, None, None, None, None, None, None) == 0
 
 
 def test_variant_switches_rejected_on_host(lib):

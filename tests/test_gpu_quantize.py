@@ -131,3 +131,43 @@ def test_quantizers_full_size_sampled(mx, orc, name):
     _check_v(mx, orc, v, windows)
     del q, k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 3, 31), (2, 3, 129), (1, 5, 300), (3, 7, 1000), (1, 2, 4096)])
+def test_quantize_qkv_one_launch_equals_single_calls(mx, B, H, N):
+    """Section 5.6's fused preprocessing: one launch writes exactly the bytes of the three single-tensor calls
+    (ragged N, one to hundreds of interleaved tiles)."""
+    q, k, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", B=B, H=H, N=N, seed=N + H)
+    fused = mx.mxattn_quantize_qkv(q, k, v)
+    single = (*mx.mxattn_rotate_quantize_qk(q), *mx.mxattn_rotate_quantize_qk(k), *mx.mxattn_quantize_v(v))
+    mx.mxattn_check()
+    for name, a, b in zip(("q_codes", "q_scales", "k_codes", "k_scales", "v_codes", "v_scales"), fused, single):
+        assert torch.equal(a, b), name
+
+
+def test_quantize_qkv_vs_oracle(mx, orc):
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=333, H=3, seed=5)
+    B, H, N, _ = q.shape
+    qc, qs, kc, ks, vc, vs = (t.cpu().numpy() for t in mx.mxattn_quantize_qkv(q, k, v))
+    mx.mxattn_check()
+    for x, c, s_ in ((q, qc, qs), (k, kc, ks)):
+        oc, os_ = orc.rotate_quantize_qk(_bits(x).reshape(B * H, N, 128))
+        assert np.array_equal(L.qk_codes_logical(c, B * H, N), oc)
+        assert np.array_equal(L.qk_scales_logical(s_, B * H, N), os_)
+    oc, os_ = orc.quantize_v(_bits(v).reshape(B * H, N, 128))
+    assert np.array_equal(L.v_codes_logical(vc, B * H, N), oc)
+    assert np.array_equal(L.v_scales_logical(vs, B * H, N), os_)
+
+
+def test_quantize_qkv_full_size_equals_single_calls(mx):
+    """At the Wan-shaped size the benchmark times: the one-launch bytes equal the single calls' bytes (which the
+    sampled oracle test above pins)."""
+    w = W.WORKLOADS["wan_32760"]
+    q, k, v = W.generate(w, device="cuda")
+    fused = mx.mxattn_quantize_qkv(q, k, v)
+    single = (*mx.mxattn_rotate_quantize_qk(q), *mx.mxattn_rotate_quantize_qk(k), *mx.mxattn_quantize_v(v))
+    mx.mxattn_check()
+    for a, b in zip(fused, single):
+        assert torch.equal(a, b)
+    del q, k, v, fused, single
+    torch.cuda.empty_cache()
