@@ -18,6 +18,11 @@ and V scales ``[BH, 128, ceil(N/32)]``.
 Scale rules: 0 = UOS (ceil, Q_max = 7.25), 1 = OCP floor, 2 = TFS (ceil, 6),
 3 = ceil with a given Q_max q in (4, 8] (the Q_max sweep of section 5.5.1).
 
+NVFP4 comparison format (section 1 and the NVFP4 baseline of section 5.2):
+16-element blocks, E4M3 block scales and a per-tensor encode factor
+e_t = 2688 / amax (readings N1-N6 in ``mxattn_oracle.c``). NVFP4 Q/K scales
+are ``[rows, 8]``, V scales ``[BH, 128, ceil(N/16)]`` (E4M3 bytes).
+
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against values and identities the pages fix (see the header of each test).
 """
@@ -82,6 +87,18 @@ def _load():
             lib.orc_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I, I, I, Dbl, I, I, P, I64, P, P, P, P]
             lib.orc_forward.restype = I
             lib.orc_sdpa.argtypes = [P, P, P, I64, I64, I, P, I64, P]
+            lib.orc_e4m3_value.argtypes = [I]
+            lib.orc_e4m3_value.restype = ctypes.c_double
+            lib.orc_e4m3_code.argtypes = [ctypes.c_double]
+            lib.orc_e4m3_code.restype = I
+            lib.orc_nvfp4_encode.argtypes = [ctypes.c_float]
+            lib.orc_nvfp4_encode.restype = ctypes.c_float
+            lib.orc_nvfp4_quantize_qk.argtypes = [P, I64, P, P, P]
+            lib.orc_nvfp4_quantize_v.argtypes = [P, I64, I64, P, P, P]
+            F32 = ctypes.c_float
+            lib.orc_forward_nvfp4.argtypes = [P, P, F32, P, P, F32, P, P, F32, P, I64, I64, I, I, I, P, I64, P, P, P,
+                                              P]
+            lib.orc_forward_nvfp4.restype = I
             lib.orc_num_threads.restype = I
             _lib = lib
     return _lib
@@ -254,3 +271,100 @@ def dequant_v(codes, scales):
     N = x.shape[1]
     s = np.repeat(np.asarray(scales, dtype=np.int64), BLOCK, axis=-1)[:, :, :N]  # [BH,128,N]
     return np.ldexp(x, np.transpose(s, (0, 2, 1)) - 127)
+
+
+# ----------------------------------------------------------------- NVFP4
+
+def e4m3_value(code: int) -> float:
+    """Value of a finite nonnegative E4M3 code (0..126)."""
+    return float(_load().orc_e4m3_value(int(code)))
+
+
+def e4m3_code(v: float) -> int:
+    """Nearest finite E4M3 code to v >= 0, ties to even, saturating at 448 (reading N1)."""
+    return int(_load().orc_e4m3_code(float(v)))
+
+
+def nvfp4_encode(amax: float) -> float:
+    """Tensor encode factor e_t = fl32(2688 / amax), 1 for an all-zero tensor (N3)."""
+    return float(_load().orc_nvfp4_encode(float(amax)))
+
+
+def nvfp4_quantize_qk(x_u16: np.ndarray):
+    """NVFP4 Q/K quantization (no rotation, N6) of bf16 bits ``[..., 128]`` as one tensor.
+
+    Returns (codes ``[..., 128]``, scales ``[..., 8]`` E4M3 bytes, e_t)."""
+    lib = _load()
+    x = _c(x_u16, np.uint16).reshape(-1, D)
+    rows = x.shape[0]
+    codes = np.empty((rows, D), dtype=np.uint8)
+    scales = np.empty((rows, D // 16), dtype=np.uint8)
+    et = np.zeros(1, dtype=np.float32)
+    lib.orc_nvfp4_quantize_qk(_p(x), rows, _p(codes), _p(scales), _p(et))
+    lead = np.shape(x_u16)[:-1]
+    return codes.reshape(*lead, D), scales.reshape(*lead, D // 16), float(et[0])
+
+
+def nvfp4_quantize_v(v_u16: np.ndarray):
+    """NVFP4 V quantization of ``[BH, N, 128]`` bf16 bits in 16-token blocks.
+
+    Returns (codes ``[BH, N, 128]``, scales ``[BH, 128, ceil(N/16)]``, e_t)."""
+    lib = _load()
+    v = _c(v_u16, np.uint16)
+    BH, N, _ = v.shape
+    nblk = (N + 15) // 16
+    codes = np.empty((BH, N, D), dtype=np.uint8)
+    scales = np.empty((BH, D, nblk), dtype=np.uint8)
+    et = np.zeros(1, dtype=np.float32)
+    lib.orc_nvfp4_quantize_v(_p(v), BH, N, _p(codes), _p(scales), _p(et))
+    return codes, scales, float(et[0])
+
+
+def forward_nvfp4(qc, qs, q_et, kc, ks, k_et, vc, vs, v_et, rows, *, vraw_u16=None, causal=False,
+                  placement=DIRECT, quant_p=True, want_phat=False):
+    """The attention loop on NVFP4 operands (logical layouts as returned above).
+
+    P~ is quantized as NVFP4 (16-key blocks, e_t = 1). ``placement``: DIRECT
+    (l from P~, the baseline's reading) or PNQ. Returns dict as :func:`forward`."""
+    lib = _load()
+    qc, qs, kc, ks, vc, vs = (_c(a, np.uint8) for a in (qc, qs, kc, ks, vc, vs))
+    BH, N, _ = qc.shape
+    vr = None if vraw_u16 is None else _c(vraw_u16, np.uint16)
+    if causal and vr is None:
+        raise ValueError("causal forward needs the unquantized V (vraw_u16)")
+    rows = _c(rows, np.int64).reshape(-1, 2)
+    R = rows.shape[0]
+    ntiles = (N + BC - 1) // BC
+    out = np.empty((R, D))
+    ell = np.empty(R)
+    phat = np.zeros((R, ntiles * BC)) if want_phat else None
+    mhist = np.full((R, ntiles), np.nan) if want_phat else None
+    rc = lib.orc_forward_nvfp4(_p(qc), _p(qs), float(q_et), _p(kc), _p(ks), float(k_et), _p(vc), _p(vs),
+                               float(v_et), _p(vr), BH, N, int(bool(causal)), int(placement), int(quant_p),
+                               _p(rows), R, _p(out), _p(ell), _p(phat), _p(mhist))
+    if rc != 0:
+        raise RuntimeError(f"orc_forward_nvfp4 failed with code {rc}")
+    res = {"out": out, "ell": ell}
+    if want_phat:
+        res["phat"] = phat
+        res["mhist"] = mhist
+    return res
+
+
+def nvfp4_dequant_qk(codes, scales, e_t):
+    """Logical NVFP4 Q/K codes + scales -> float64 ``[..., 128]``."""
+    vals = np.array([e2m1_value(c) for c in range(16)])
+    svals = np.array([e4m3_value(c) if c < 127 else np.nan for c in range(256)])
+    x = vals[np.asarray(codes)]
+    s = np.repeat(svals[np.asarray(scales)], 16, axis=-1)
+    return x * s / e_t
+
+
+def nvfp4_dequant_v(codes, scales, e_t):
+    """Logical NVFP4 V codes ``[BH, N, 128]`` + scales ``[BH, 128, nblk]`` -> float64 ``[BH, N, 128]``."""
+    vals = np.array([e2m1_value(c) for c in range(16)])
+    svals = np.array([e4m3_value(c) if c < 127 else np.nan for c in range(256)])
+    x = vals[np.asarray(codes)]
+    N = x.shape[1]
+    s = np.repeat(svals[np.asarray(scales)], 16, axis=-1)[:, :, :N]
+    return x * np.transpose(s, (0, 2, 1)) / e_t

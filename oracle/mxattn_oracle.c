@@ -28,6 +28,26 @@
  *       V block that holds the query itself, P^ multiplies the unquantized
  *       (bf16) V rows instead of V^, so no later token can reach row i.
  *
+ * NVFP4 comparison format (section 1: E2M1 values in 16-element blocks with
+ * an E4M3 block scale and a tensor-level scale; section 5.2: the direct NVFP4
+ * baseline quantizes Q, K, V and P~ for the two products, with no smoothing
+ * and no softmax-path scaling):
+ *   N1  E4M3 block scales: round to nearest, ties to the even code, values at
+ *       or above 448 saturate to 448 (the largest finite E4M3 value).
+ *   N2  A block's scale maps its maximum |x| to the E2M1 maximum 6.
+ *   N3  Tensor scale of Q, K, V: encode factor e_t = 2688 / amax over the
+ *       whole tensor (2688 = 6 * 448), so the largest block scale is 448;
+ *       e_t = 1 if the tensor is all zero. P~ has no tensor scale (e_t = 1).
+ *   N4  Binary32 order of operations (the GPU quantizers use the same):
+ *         e_t = fl(2688 / amax)
+ *         sc  = E4M3(fl(fl(M / 6) * e_t)), S = value of sc
+ *         sc == 0: every code 0; else k = fl(e_t / S), code = E2M1(fl(x * k))
+ *       dequantized value = E2M1 value * S / e_t.
+ *   N5  Blocks of 16: Q/K per token over channels [16b, 16b+16), V per
+ *       channel over tokens [16t, 16t+16), P~ per row over keys [16t, 16t+16).
+ *       Causal: the query's own 16-token V block uses the bf16 V rows (R6).
+ *   N6  Q and K are not rotated.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared [-fopenmp] -lm
  */
 #include <math.h>
@@ -124,6 +144,61 @@ static float bf16_to_f32(uint16_t b) {
   return f;
 }
 
+/* ---------------------------------------------------------- E4M3 (N1)
+ * Finite nonnegative E4M3 codes 0..126 (0x7F is NaN): exponent field
+ * c >> 3, mantissa c & 7; field 0 is subnormal (m/8 * 2^-6), else
+ * (1 + m/8) * 2^(field - 7). Largest finite value: code 126 = 448.          */
+double orc_e4m3_value(int code) {
+  const int ef = (code >> 3) & 15, m = code & 7;
+  if (ef == 0) return ldexp((double)m, -9);
+  return ldexp(8.0 + m, ef - 10);
+}
+
+/* Nearest finite E4M3 code to v >= 0, ties to the even code; >= 448 -> 126. */
+int orc_e4m3_code(double v) {
+  if (!(v < 448.0)) return 126;
+  int best = 0;
+  double bestd = fabs(v);
+  for (int c = 1; c <= 126; c++) {
+    const double d = fabs(v - orc_e4m3_value(c));
+    if (d < bestd || (d == bestd && (c % 2) == 0 && (best % 2) != 0)) {
+      best = c;
+      bestd = d;
+    }
+  }
+  return best;
+}
+
+/* Tensor encode factor e_t (N3, N4). */
+float orc_nvfp4_encode(float amax) { return amax > 0.0f ? 2688.0f / amax : 1.0f; }
+
+/* Quantize one block of n binary32 values with encode factor e_t (N2, N4).
+ * codes[i] receives the 4-bit code; returns the E4M3 scale byte.           */
+static int nv_block(const float* x, int n, float e_t, uint8_t* codes) {
+  float M = 0.0f;
+  for (int i = 0; i < n; i++)
+    if (fabsf(x[i]) > M) M = fabsf(x[i]);
+  const float t = M / 6.0f;
+  const float v = t * e_t;
+  const int sc = orc_e4m3_code((double)v);
+  const float S = (float)orc_e4m3_value(sc);
+  if (sc == 0) {
+    for (int i = 0; i < n; i++) codes[i] = 0;
+    return 0;
+  }
+  const float k = e_t / S;
+  for (int i = 0; i < n; i++) {
+    const float y = x[i] * k;
+    codes[i] = (uint8_t)orc_e2m1_code((double)y);
+  }
+  return sc;
+}
+
+/* Dequantized NVFP4 element: E2M1 value * S / e_t, in float64. */
+static double nv_dq(uint8_t code, uint8_t sc, float e_t) {
+  return orc_e2m1_value(code) * orc_e4m3_value(sc) / (double)e_t;
+}
+
 /* ------------------------------------------------------ Hadamard (R2)
  * y = x R_H with R_H = H_128 / sqrt(128), Sylvester order. Binary32.       */
 void orc_hadamard_fp32(const uint16_t* x_bf16, float* y) {
@@ -186,6 +261,52 @@ void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, double q
   }
 }
 
+/* ------------------------------------------- NVFP4 Q/K and V (N1-N6)
+ * Q/K: x [rows][128] bf16; codes [rows][128] one per byte; scales [rows][8]
+ * E4M3 bytes (16-channel blocks); *e_t: the tensor's encode factor.         */
+void orc_nvfp4_quantize_qk(const uint16_t* x, int64_t rows, uint8_t* codes, uint8_t* scales, float* e_t) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < rows * ORC_D; i++) {
+    const float a = fabsf(bf16_to_f32(x[i]));
+    if (a > amax) amax = a;
+  }
+  const float et = orc_nvfp4_encode(amax);
+  *e_t = et;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; r++) {
+    float v[ORC_D];
+    for (int c = 0; c < ORC_D; c++) v[c] = bf16_to_f32(x[r * ORC_D + c]);
+    for (int b = 0; b < ORC_D / 16; b++) scales[r * 8 + b] = (uint8_t)nv_block(v + 16 * b, 16, et, codes + r * ORC_D + 16 * b);
+  }
+}
+
+/* V: v [BH][N][128] bf16; codes [BH][N][128]; scales [BH][128][ceil(N/16)]
+ * (16-token blocks per channel, the last one short); *e_t as above.        */
+void orc_nvfp4_quantize_v(const uint16_t* v, int64_t BH, int64_t N, uint8_t* codes, uint8_t* scales, float* e_t) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < BH * N * ORC_D; i++) {
+    const float a = fabsf(bf16_to_f32(v[i]));
+    if (a > amax) amax = a;
+  }
+  const float et = orc_nvfp4_encode(amax);
+  *e_t = et;
+  const int64_t nblk = (N + 15) / 16;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t bh = 0; bh < BH; bh++) {
+    for (int c = 0; c < ORC_D; c++) {
+      for (int64_t t = 0; t < nblk; t++) {
+        const int64_t n0 = t * 16;
+        const int n = (int)(N - n0 < 16 ? N - n0 : 16);
+        float vals[16];
+        uint8_t cb[16];
+        for (int i = 0; i < n; i++) vals[i] = bf16_to_f32(v[(bh * N + n0 + i) * ORC_D + c]);
+        scales[(bh * ORC_D + c) * nblk + t] = (uint8_t)nv_block(vals, n, et, cb);
+        for (int i = 0; i < n; i++) codes[(bh * N + n0 + i) * ORC_D + c] = cb[i];
+      }
+    }
+  }
+}
+
 /* ------------------------------------------------ online softmax core
  * Algorithm 2 (section 4.3) loop, Eqs. 2-8 with PNQ (Eqs. 44-48), for one query row against one head's keys, float64.
  *   q      : 128 query values (already dequantized)
@@ -198,7 +319,9 @@ void orc_quantize_v(const uint16_t* v, int64_t BH, int64_t N, int rule, double q
  * tokens b0..i only (tokens after i left out of the block maximum), using the
  * P~ rule p_rule / p_q.
  * Options: quant_p (PNQ quantizer on), placement (0 = PNQ: l from P^,
- * 1 = direct: l from P~, Eq. 16-17), p_rule (scale rule for P~), bc (tile).
+ * 1 = direct: l from P~, Eq. 16-17), p_rule (scale rule for P~), bc (tile),
+ * nv (P~ as NVFP4: 16-key blocks with the E4M3 scale of M/6, and the
+ * causal diagonal block is the query's own 16-token V block).
  * Outputs: o[128], *ell; optional phat[ntiles*bc] (P^ of each tile before any
  * later rescale, masked slots 0) and mhist[ntiles] (running max after each
  * tile).                                                                    */
@@ -209,6 +332,7 @@ typedef struct {
   int p_rule;
   int bc;
   double p_q;
+  int nv; /* 1: P~ quantized as NVFP4 (16-key blocks, E4M3 scale of M/6, N1-N5) */
 } orc_opts;
 
 static void online_softmax_row(const double* q, const double* K, const double* V, const double* Vraw,
@@ -260,29 +384,43 @@ static void online_softmax_row(const double* q, const double* K, const double* V
     double alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
     /* Eq. 5: P~ = exp(S - m_new) */
     for (int kk = 0; kk < bc; kk++) Pt[kk] = valid[kk] ? exp(S[kk] - m_new) : 0.0;
-    /* Eq. 44: P^ = Q*(P~), 32-key blocks counted from key 0 */
-    for (int b0 = 0; b0 < bc; b0 += ORC_BLOCK) {
-      if (op->quant_p) {
+    /* Eq. 44: P^ = Q*(P~), 32-key blocks counted from key 0 (16 for NVFP4) */
+    const int pblk = op->nv ? 16 : ORC_BLOCK;
+    for (int b0 = 0; b0 < bc; b0 += pblk) {
+      if (op->quant_p && op->nv) {
+        /* N2, N4 with e_t = 1, in float64: S = E4M3(fl(M / 6)), code = E2M1(P~ / S) */
+        double M = 0.0;
+        for (int t = 0; t < 16; t++)
+          if (Pt[b0 + t] > M) M = Pt[b0 + t];
+        const int sc = orc_e4m3_code((double)(float)(M / 6.0));
+        const double S = orc_e4m3_value(sc);
+        for (int t = 0; t < 16; t++)
+          Ph[b0 + t] = sc == 0 ? 0.0 : orc_e2m1_value(orc_e2m1_code(Pt[b0 + t] / S)) * S;
+      } else if (op->quant_p) {
         uint8_t cb[ORC_BLOCK];
         int sb = quantize_block(Pt + b0, ORC_BLOCK, op->p_rule, op->p_q, cb);
         for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = dq(cb[t], (uint8_t)sb);
       } else {
-        for (int t = 0; t < ORC_BLOCK; t++) Ph[b0 + t] = Pt[b0 + t];
+        for (int t = 0; t < pblk; t++) Ph[b0 + t] = Pt[b0 + t];
       }
     }
     /* Eq. 47 (PNQ) or Eq. 16 (direct placement) */
     double tile_sum = 0.0;
     for (int kk = 0; kk < bc; kk++) tile_sum += (op->placement == 0) ? Ph[kk] : Pt[kk];
     ell = alpha * ell + tile_sum;
-    /* Eq. 48: O = diag(alpha) O + P^ V^ */
-    for (int c = 0; c < ORC_D; c++) acc[c] *= alpha;
+    /* Eq. 48: O = diag(alpha) O + P^ V^_j -- the tile product P^ V^_j first,
+     * then the update, as l = alpha l + sum P^ above */
+    double tp[ORC_D];
+    for (int c = 0; c < ORC_D; c++) tp[c] = 0.0;
     for (int kk = 0; kk < bc; kk++) {
       if (!valid[kk] || Ph[kk] == 0.0) continue;
       int64_t key = k0 + kk;
-      const int diag = op->causal && (key / ORC_BLOCK) == (i / ORC_BLOCK);
+      const int vblk = op->nv ? 16 : ORC_BLOCK;
+      const int diag = op->causal && (key / vblk) == (i / vblk);
       const double* vrow = !diag ? V + key * ORC_D : (op->causal == 2 ? Vd + (key - b0) * ORC_D : Vraw + key * ORC_D);
-      for (int c = 0; c < ORC_D; c++) acc[c] += Ph[kk] * vrow[c];
+      for (int c = 0; c < ORC_D; c++) tp[c] += Ph[kk] * vrow[c];
     }
+    for (int c = 0; c < ORC_D; c++) acc[c] = alpha * acc[c] + tp[c];
     m = m_new;
     if (phat) memcpy(phat + j * bc, Ph, sizeof(double) * bc);
     if (mhist) mhist[j] = m;
@@ -304,7 +442,7 @@ void orc_online_softmax(const double* q_rows, const int64_t* row_tok, int64_t nr
                         const double* V, const double* Vraw, int64_t N, int causal, int quant_p,
                         int placement, int p_rule, double p_q, int bc, double* out, double* ell, double* phat,
                         double* mhist) {
-  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0};
   const int64_t ntiles = (N + bc - 1) / bc;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; r++) {
@@ -328,7 +466,7 @@ int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const u
   if (bc <= 0 || bc % ORC_BLOCK != 0) return 1;
   const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
   const int64_t ntiles = (N + bc - 1) / bc;
-  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0};
   double* K = (double*)malloc(sizeof(double) * N * ORC_D);
   double* V = (double*)malloc(sizeof(double) * N * ORC_D);
   double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);
@@ -359,6 +497,61 @@ int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const u
       for (int c = 0; c < ORC_D; c++) {
         const int64_t e = (bh * N + i) * ORC_D + c;
         q[c] = dq(qc[e], qs[(bh * N + i) * 4 + c / ORC_BLOCK]);
+      }
+      online_softmax_row(q, K, V, Vr, N, i, &op, out + r * ORC_D, ell + r,
+                         phat ? phat + r * ntiles * bc : NULL, mhist ? mhist + r * ntiles : NULL);
+    }
+  }
+  free(K);
+  free(V);
+  free(Vr);
+  return 0;
+}
+
+/* ------------------------------------------------ NVFP4 forward (N1-N6)
+ * The same loop with NVFP4 operands: qc, kc, vc [BH][N][128] codes; qs, ks
+ * [BH][N][8] E4M3 bytes; vs [BH][128][ceil(N/16)]; q_et, k_et, v_et the
+ * tensors' encode factors. causal 0 or 1 (the own 16-token V block on bf16).
+ * P~ is NVFP4-quantized when quant_p (N2, N4 with e_t = 1).                  */
+int orc_forward_nvfp4(const uint8_t* qc, const uint8_t* qs, float q_et, const uint8_t* kc, const uint8_t* ks,
+                      float k_et, const uint8_t* vc, const uint8_t* vs, float v_et, const uint16_t* vraw, int64_t BH,
+                      int64_t N, int causal, int placement, int quant_p, const int64_t* rows, int64_t nrows,
+                      double* out, double* ell, double* phat, double* mhist) {
+  if (causal != 0 && causal != 1) return 1;
+  const int bc = 128;
+  const int64_t nblk = (N + 15) / 16;
+  const int64_t ntiles = (N + bc - 1) / bc;
+  orc_opts op = {causal, quant_p, placement, 0, bc, 7.25, 1};
+  double* K = (double*)malloc(sizeof(double) * N * ORC_D);
+  double* V = (double*)malloc(sizeof(double) * N * ORC_D);
+  double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);
+  if (!K || !V || !Vr) {
+    free(K);
+    free(V);
+    free(Vr);
+    return 2;
+  }
+  for (int64_t bh = 0; bh < BH; bh++) {
+    int any = 0;
+    for (int64_t r = 0; r < nrows; r++) any |= (rows[2 * r] == bh);
+    if (!any) continue;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++) {
+      for (int c = 0; c < ORC_D; c++) {
+        const int64_t e = (bh * N + n) * ORC_D + c;
+        K[n * ORC_D + c] = nv_dq(kc[e], ks[(bh * N + n) * 8 + c / 16], k_et);
+        V[n * ORC_D + c] = nv_dq(vc[e], vs[(bh * ORC_D + c) * nblk + n / 16], v_et);
+        Vr[n * ORC_D + c] = vraw ? (double)bf16_to_f32(vraw[e]) : V[n * ORC_D + c];
+      }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; r++) {
+      if (rows[2 * r] != bh) continue;
+      const int64_t i = rows[2 * r + 1];
+      double q[ORC_D];
+      for (int c = 0; c < ORC_D; c++) {
+        const int64_t e = (bh * N + i) * ORC_D + c;
+        q[c] = nv_dq(qc[e], qs[(bh * N + i) * 8 + c / 16], q_et);
       }
       online_softmax_row(q, K, V, Vr, N, i, &op, out + r * ORC_D, ell + r,
                          phat ? phat + r * ntiles * bc : NULL, mhist ? mhist + r * ntiles : NULL);
