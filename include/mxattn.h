@@ -179,6 +179,27 @@ MXATTN_API mxattn_status mxattn_forward_ex(const void* q_codes, const void* q_sc
                                            const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                                            int p_rule, double p_qmax, int placement, float* out, void* stream);
 
+/* NVFP4 comparison path ("MXAttention" section 1: E2M1 values in 16-element
+ * blocks with an E4M3 block scale and a tensor-level scale; section 5.2: the
+ * direct NVFP4 baseline quantizes Q, K, V and P~ for the two products, with no
+ * smoothing and no softmax-path scaling). Each quantizer first writes the
+ * tensor's max |x| to *amax (device float, 4 bytes), then quantizes with the
+ * encode factor e_t = fl32(2688 / amax) (2688 = 6 * 448): per block of 16,
+ *   sc = E4M3(fl32(fl32(M / 6) * e_t))   (round to nearest even, saturate at 448)
+ *   code = E2M1(fl32(x * fl32(e_t / value(sc))))   (every code 0 when sc == 0)
+ * Q and K are not rotated. Codes use the MXFP4 layouts (mxattn_qk_codes_bytes,
+ * mxattn_v_codes_bytes; V blocks run along tokens). Scales: E4M3 bytes, two
+ * 512-byte atoms per 128-row tile (mxattn_nvfp4_scales_bytes), atom kk holding
+ * blocks 4kk .. 4kk+3 of row r at byte (r%32)*16 + (r/32)*4 + (block % 4);
+ * rows are tokens for Q/K (blocks over channels) and channels for V (blocks
+ * over the tile's tokens). Outputs must not overlap the input or each other.
+ * Two launches and a 4-byte memset per call, on `stream`. */
+MXATTN_API size_t mxattn_nvfp4_scales_bytes(int64_t B, int64_t H, int64_t N); /* B*H*ceil(N/128)*1024 */
+MXATTN_API mxattn_status mxattn_nvfp4_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D,
+                                                  void* codes, void* scales, float* amax, void* stream);
+MXATTN_API mxattn_status mxattn_nvfp4_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D,
+                                                 void* codes, void* scales, float* amax, void* stream);
+
 /* Device workspace needed by mxattn_attention_host for [B, H, N, 128]. */
 MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);
 

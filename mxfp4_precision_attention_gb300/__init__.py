@@ -20,7 +20,8 @@ __all__ = [
     "MxattnError", "load", "mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_quantize_qkv", "mxattn_forward",
     "mxattn_forward_dump_phat", "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_workspace_bytes",
     "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
-    "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes",
+    "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes", "mxattn_nvfp4_quantize_qk",
+    "mxattn_nvfp4_quantize_v",
 ]
 
 D = 128
@@ -57,6 +58,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_rotate_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P]
         lib.mxattn_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P]
         lib.mxattn_quantize_qkv.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, P, P, P]
+        lib.mxattn_nvfp4_scales_bytes.argtypes = [I64, I64, I64]
+        lib.mxattn_nvfp4_scales_bytes.restype = SZ
+        lib.mxattn_nvfp4_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
+        lib.mxattn_nvfp4_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
@@ -150,6 +155,28 @@ def mxattn_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out=N
     _raise(load().mxattn_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, *(_ptr(t) for t in out),
                                       _stream(stream)))
     return tuple(out)
+
+
+def mxattn_nvfp4_quantize_qk(x: torch.Tensor, stream=None):
+    """NVFP4 Q/K quantization (no rotation). Returns (codes, scales, amax): uint8, uint8, fp32 [1]."""
+    B, H, N, Dx = _shape(x)
+    codes = torch.empty(qk_layout_sizes(B, H, N)[0], dtype=torch.uint8, device=x.device)
+    scales = torch.empty(int(load().mxattn_nvfp4_scales_bytes(B, H, N)), dtype=torch.uint8, device=x.device)
+    amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _raise(load().mxattn_nvfp4_quantize_qk(_ptr(x), B, H, N, Dx, _ptr(codes), _ptr(scales), _ptr(amax),
+                                           _stream(stream)))
+    return codes, scales, amax
+
+
+def mxattn_nvfp4_quantize_v(v: torch.Tensor, stream=None):
+    """NVFP4 V quantization (16-token blocks). Returns (codes, scales, amax)."""
+    B, H, N, Dx = _shape(v)
+    codes = torch.empty(v_layout_sizes(B, H, N)[0], dtype=torch.uint8, device=v.device)
+    scales = torch.empty(int(load().mxattn_nvfp4_scales_bytes(B, H, N)), dtype=torch.uint8, device=v.device)
+    amax = torch.empty(1, dtype=torch.float32, device=v.device)
+    _raise(load().mxattn_nvfp4_quantize_v(_ptr(v), B, H, N, Dx, _ptr(codes), _ptr(scales), _ptr(amax),
+                                          _stream(stream)))
+    return codes, scales, amax
 
 
 def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,

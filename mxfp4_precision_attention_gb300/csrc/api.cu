@@ -262,6 +262,9 @@ using namespace mxattn;
 
 extern "C" {
 
+size_t mxattn_nvfp4_scales_bytes(int64_t B, int64_t H, int64_t N) {
+  return B < 0 || H < 0 || N < 0 ? 0 : 2 * sf_bytes(B, H, N);
+}
 size_t mxattn_qk_codes_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : qk_codes(B, H, N); }
 size_t mxattn_qk_scales_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : sf_bytes(B, H, N); }
 size_t mxattn_v_codes_bytes(int64_t B, int64_t H, int64_t N) { return B < 0 || H < 0 || N < 0 ? 0 : v_codes(B, H, N); }
@@ -317,6 +320,39 @@ mxattn_status mxattn_quantize_v_ex(const void* v, int64_t B, int64_t H, int64_t 
   return MXATTN_OK;
 }
 
+static mxattn_status nvfp4_quantize(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                    void* scales, float* amax, void* stream, int is_v) {
+  t_err[0] = '\0';
+  bool empty = false;
+  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (empty) return MXATTN_OK;
+  MX_TRY(check_ptr(x, "x"));
+  MX_TRY(check_ptr(codes, "codes"));
+  MX_TRY(check_ptr(scales, "scales"));
+  if (amax == nullptr || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return fail(MXATTN_ERR_INVALID_ARG, "amax must be a non-NULL, 4-byte aligned device float");
+  const size_t nc = is_v ? v_codes(B, H, N) : qk_codes(B, H, N);
+  const Range rx = rng(x, bf16_bytes(B, H, N)), rc = rng(codes, nc), rs = rng(scales, 2 * sf_bytes(B, H, N)),
+              ra = rng(amax, sizeof(float));
+  if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs) || overlap(ra, rx) || overlap(ra, rc) || overlap(ra, rs))
+    return fail(MXATTN_ERR_INVALID_ARG, "x, codes, scales and amax must not overlap");
+  MX_TRY(check_quantizer_runtime());
+  const QuantizeJob j{x, codes, scales, kRuleUOS, 7.25, is_v, 0, amax};
+  cudaError_t e = launch_quantize(&j, 1, B * H, N, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "nvfp4 quantizer launch");
+  return MXATTN_OK;
+}
+
+mxattn_status mxattn_nvfp4_quantize_qk(const void* x, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                       void* scales, float* amax, void* stream) {
+  return nvfp4_quantize(x, B, H, N, D, codes, scales, amax, stream, 0);
+}
+
+mxattn_status mxattn_nvfp4_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D, void* codes,
+                                      void* scales, float* amax, void* stream) {
+  return nvfp4_quantize(v, B, H, N, D, codes, scales, amax, stream, 1);
+}
+
 mxattn_status mxattn_quantize_qkv(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
                                   int64_t D, void* q_codes, void* q_scales, void* k_codes, void* k_scales,
                                   void* v_codes, void* v_scales, void* stream) {
@@ -345,9 +381,9 @@ mxattn_status mxattn_quantize_qkv(const void* q, const void* k, const void* v, i
       if (overlap(outs[i], outs[j])) return fail(MXATTN_ERR_INVALID_ARG, "two outputs overlap");
   }
   MX_TRY(check_quantizer_runtime());
-  const QuantizeJob jobs[3] = {{q, q_codes, q_scales, kRuleUOS, 7.25, 0, 1},
-                               {k, k_codes, k_scales, kRuleUOS, 7.25, 0, 1},
-                               {v, v_codes, v_scales, kRuleUOS, 7.25, 1, 0}};
+  const QuantizeJob jobs[3] = {{q, q_codes, q_scales, kRuleUOS, 7.25, 0, 1, nullptr},
+                               {k, k_codes, k_scales, kRuleUOS, 7.25, 0, 1, nullptr},
+                               {v, v_codes, v_scales, kRuleUOS, 7.25, 1, 0, nullptr}};
   cudaError_t e = launch_quantize(jobs, 3, B * H, N, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_qkv launch");
   return MXATTN_OK;

@@ -37,6 +37,7 @@ struct QuantizeJob {
   double qmax;
   int is_v;
   int rotate;
+  float* amax;  // non-null: NVFP4 (16-element blocks, E4M3 scales), tensor max |x| written here
 };
 // Up to three jobs of the same B*H and N in one launch (their tiles interleave).
 cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int64_t N, cudaStream_t s);

@@ -155,6 +155,8 @@ struct QTensor {
   ScaleRule rule;
   int is_v;    // 0: Q/K (per-token channel blocks), 1: V (per-channel token blocks)
   int rotate;  // Q/K only
+  int nv;      // 1: NVFP4 (16-element blocks, E4M3 scales; no rotation)
+  const float* amax;  // NVFP4: the tensor's max |x| (written by the amax pass)
 };
 struct QParams {
   QTensor t[3];
@@ -163,6 +165,174 @@ struct QParams {
   int64_t units;                 // ntensors * BH * NT
   int* status;
 };
+
+// ----------------------------------------------------------------- NVFP4
+// NVFP4 ("MXAttention" section 1: E2M1 values in 16-element blocks, an E4M3
+// block scale and a tensor-level scale) with the binary32 order of operations
+// the comparison baseline fixes:
+//   e_t = fl(2688 / amax)  (2688 = 6 * 448; 1 for an all-zero tensor)
+//   sc  = E4M3(fl(fl(M / 6) * e_t)), round to nearest even, saturating at 448
+//   sc == 0: every code 0; else k = fl(e_t / value(sc)), code = E2M1(fl(x * k))
+// Scales: two 512-byte atoms per 128-row tile, atom kk holding blocks
+// 4kk .. 4kk+3 (the K range of one 64-wide MMA) at byte
+// (r%32)*16 + (r/32)*4 + (block % 4).
+__device__ __forceinline__ float nv_encode(const float* amax) {
+  const float a = __ldg(amax);
+  return a > 0.0f ? __fdiv_rn(2688.0f, a) : 1.0f;
+}
+
+// E4M3 code (round to nearest even, saturating at 448) of v >= 0.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(v));
+  return h & 0xFFu;
+}
+
+// Value of a finite nonnegative E4M3 code.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t ef = (c >> 3) & 15u, m = c & 7u;
+  return ef ? __uint_as_float(((ef + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0x1p-9f;
+}
+
+// Block scale code and element factor of a block maximum M.
+__device__ __forceinline__ uint32_t nv_block_scale(float M, float et, float* k) {
+  const uint32_t sc = e4m3_code(__fmul_rn(__fdiv_rn(M, 6.0f), et));
+  *k = sc ? __fdiv_rn(et, e4m3_value(sc)) : 0.0f;
+  return sc;
+}
+
+__device__ __forceinline__ float absmax16(const float* v) {
+  const float a0 = max3f(fabsf(v[0]), fabsf(v[1]), fabsf(v[2])), a1 = max3f(fabsf(v[3]), fabsf(v[4]), fabsf(v[5]));
+  const float a2 = max3f(fabsf(v[6]), fabsf(v[7]), fabsf(v[8])), a3 = max3f(fabsf(v[9]), fabsf(v[10]), fabsf(v[11]));
+  const float a4 = max3f(fabsf(v[12]), fabsf(v[13]), fabsf(v[14]));
+  return max3f(max3f(a0, a1, a2), max3f(a3, a4, fabsf(v[15])), 0.0f);
+}
+
+// NVFP4 Q/K tile: one thread per token, 8 blocks of 16 channels.
+__device__ __forceinline__ void quantize_qk_tile_nv(const uint8_t* tile, int r, int64_t bh, int64_t t,
+                                                    const QParams& p, const QTensor& T, uint32_t empty_bar) {
+  float z[kD];
+#pragma unroll
+  for (int c = 0; c < kD / 8; c++) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kQHalfBytes + r * 128 +
+                                                      (((c & 7) ^ (r & 7)) << 4));
+    bf16x2_to_f32(raw.x, z[8 * c + 0], z[8 * c + 1]);
+    bf16x2_to_f32(raw.y, z[8 * c + 2], z[8 * c + 3]);
+    bf16x2_to_f32(raw.z, z[8 * c + 4], z[8 * c + 5]);
+    bf16x2_to_f32(raw.w, z[8 * c + 6], z[8 * c + 7]);
+  }
+  __syncwarp();
+  if ((r & 31) == 0) mbar_arrive(empty_bar);
+  const float et = nv_encode(T.amax);
+  const int64_t n = t * kTile + r;
+  const bool real = n < p.N;
+  uint2* crow = reinterpret_cast<uint2*>(T.codes) + (bh * p.N + n) * (kD / 16);
+  uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+  for (int b = 0; b < kD / 16; b++) {
+    const float* c = z + 16 * b;
+    float k;
+    const uint32_t sc = nv_block_scale(absmax16(c), et, &k);
+    uint32_t w[2];
+#pragma unroll
+    for (int g = 0; g < 2; g++) {
+      const float* cg = c + 8 * g;
+      w[g] = pack_e2m1x8(__fmul_rn(cg[0], k), __fmul_rn(cg[1], k), __fmul_rn(cg[2], k), __fmul_rn(cg[3], k),
+                         __fmul_rn(cg[4], k), __fmul_rn(cg[5], k), __fmul_rn(cg[6], k), __fmul_rn(cg[7], k));
+    }
+    if (sc == 0u) w[0] = w[1] = 0u;
+    if (real) crow[b] = make_uint2(w[0], w[1]);
+    sw[b / 4] |= sc << (8 * (b % 4));
+  }
+  uint32_t* atom = T.scales + (bh * p.NT + t) * (2 * kSfAtomBytes / 4);
+  atom[(r % 32) * 4 + (r / 32)] = sw[0];
+  atom[kSfAtomBytes / 4 + (r % 32) * 4 + (r / 32)] = sw[1];
+}
+
+// NVFP4 V tile: warp kb takes tokens 32kb .. 32kb+31 (two 16-token blocks);
+// lane l owns channels 2l, 2l+1, 64+2l, 65+2l.
+__device__ __forceinline__ void quantize_v_tile_nv(const uint8_t* tile, int kb, int lane, int64_t bh, int64_t t,
+                                                   const QParams& p, const QTensor& T, uint32_t empty_bar) {
+  uint32_t w[2][kBlock];
+#pragma unroll
+  for (int i = 0; i < kBlock; i++) {
+    const int row = kb * kBlock + i;
+    const int off = row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) + ((lane & 3) << 2);
+    w[0][i] = *reinterpret_cast<const uint32_t*>(tile + off);
+    w[1][i] = *reinterpret_cast<const uint32_t*>(tile + kQHalfBytes + off);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+  const float et = nv_encode(T.amax);
+  const int64_t tok0 = t * kTile + kb * kBlock;
+  uint8_t* sbytes = reinterpret_cast<uint8_t*>(T.scales + (bh * p.NT + t) * (2 * kSfAtomBytes / 4)) +
+                    (kb / 2) * kSfAtomBytes;
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    uint32_t cw[2][4];
+    const int c0 = 64 * h + 2 * lane;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {  // tokens 16j .. 16j+15 of the warp's 32
+      uint32_t mw = w[h][16 * j] & 0x7FFF7FFFu;
+#pragma unroll
+      for (int i = 1; i < 16; i++) {
+        const uint32_t a = w[h][16 * j + i] & 0x7FFF7FFFu;
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(mw) : "r"(a));
+      }
+      float m2[2];
+      bf16x2_to_f32(mw, m2[0], m2[1]);
+      float k2[2];
+      uint32_t sc[2];
+#pragma unroll
+      for (int q = 0; q < 2; q++) sc[q] = nv_block_scale(m2[q], et, &k2[q]);
+#pragma unroll
+      for (int g = 0; g < 2; g++) {
+        float q0[8], q1[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          float lo, hi;
+          bf16x2_to_f32(w[h][16 * j + 8 * g + i], lo, hi);
+          q0[i] = __fmul_rn(lo, k2[0]);
+          q1[i] = __fmul_rn(hi, k2[1]);
+        }
+        cw[0][2 * j + g] = sc[0] ? pack_e2m1x8(q0[0], q0[1], q0[2], q0[3], q0[4], q0[5], q0[6], q0[7]) : 0u;
+        cw[1][2 * j + g] = sc[1] ? pack_e2m1x8(q1[0], q1[1], q1[2], q1[3], q1[4], q1[5], q1[6], q1[7]) : 0u;
+      }
+      // block 2*kb + j of the tile -> atom kb/2, byte 2*(kb%2) + j
+#pragma unroll
+      for (int q = 0; q < 2; q++) {
+        const int c = c0 + q;
+        sbytes[(c % 32) * 16 + (c / 32) * 4 + 2 * (kb % 2) + j] = static_cast<uint8_t>(sc[q]);
+      }
+    }
+    if (tok0 < p.N) {
+#pragma unroll
+      for (int q = 0; q < 2; q++)
+        *reinterpret_cast<uint4*>(T.codes + (bh * kD + c0 + q) * p.row_bytes + tok0 / 2) =
+            make_uint4(cw[q][0], cw[q][1], cw[q][2], cw[q][3]);
+    }
+  }
+}
+
+// max |x| of a bf16 tensor into *amax_bits (zeroed before the launch): the
+// bits of a nonnegative binary32 order like the values.
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                   uint32_t* __restrict__ amax_bits) {
+  uint32_t m = 0u;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 u = __ldg(x + i);
+    const uint32_t a[4] = {u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu, u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu};
+#pragma unroll
+    for (int j = 0; j < 4; j++) asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(a[j]));
+  }
+  float lo, hi;
+  bf16x2_to_f32(m, lo, hi);
+  float f = fmaxf(lo, hi);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, d));
+  if ((threadIdx.x & 31) == 0 && f > 0.0f) atomicMax(amax_bits, __float_as_uint(f));
+}
 
 __device__ __forceinline__ void quantize_qk_tile(const uint8_t* tile, int r, int64_t bh, int64_t t, const QParams& p,
                                                  const QTensor& T, uint32_t empty_bar) {
@@ -358,10 +528,16 @@ __global__ void __launch_bounds__(kQThreads, kQMinBlocks)
     // a copy picked by value: a run-time index into the parameter array would go through local memory
     const QTensor T = ti == 0 ? p.t[0] : (ti == 1 ? p.t[1] : p.t[2]);
     const uint8_t* st = smem + s * kQStageBytes;
-    if (T.is_v)
+    if (T.nv) {
+      if (T.is_v)
+        quantize_v_tile_nv(st, warp, lane, bh, t, p, T, empty(s));
+      else
+        quantize_qk_tile_nv(st, threadIdx.x, bh, t, p, T, empty(s));
+    } else if (T.is_v) {
       quantize_v_tile(st, warp, lane, bh, t, p, T, empty(s));
-    else
+    } else {
       quantize_qk_tile(st, threadIdx.x, bh, t, p, T, empty(s));
+    }
   }
   // after an abort, every copy the leader issued must land before the CTA exits
   if (leader && *abort_flag) {
@@ -393,6 +569,8 @@ cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int6
     p.t[j].rule = make_rule(jobs[j].rule, jobs[j].qmax);
     p.t[j].is_v = jobs[j].is_v;
     p.t[j].rotate = jobs[j].rotate;
+    p.t[j].nv = jobs[j].amax != nullptr;
+    p.t[j].amax = jobs[j].amax;
   }
   for (int j = njobs; j < 3; j++) maps[j] = maps[0];
   p.ntensors = njobs;
@@ -418,6 +596,19 @@ cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int6
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
+  // NVFP4 jobs: the tensor maximum first (the encode factor needs it)
+  for (int j = 0; j < njobs; j++) {
+    if (jobs[j].amax == nullptr) continue;
+    e = cudaMemsetAsync(jobs[j].amax, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    const int64_t nvec = BH * N * (kD / 8);
+    const int64_t blocks = ceil_div(nvec, 256);
+    const int agrid = static_cast<int>(blocks < 8 * sms[dev] ? blocks : 8 * sms[dev]);
+    amax_kernel<<<agrid, 256, 0, s>>>(static_cast<const uint4*>(jobs[j].x), nvec,
+                                      reinterpret_cast<uint32_t*>(jobs[j].amax));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // persistent: as many CTAs per SM as registers and shared memory allow
   const int64_t want = kQMinBlocks * static_cast<int64_t>(sms[dev]);
   const int grid = static_cast<int>(p.units < want ? p.units : want);
@@ -427,13 +618,13 @@ cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int6
 
 cudaError_t launch_rotate_quantize_qk(const void* x, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                                       double qmax, int rotate, cudaStream_t s) {
-  const QuantizeJob j{x, codes, scales, rule, qmax, 0, rotate};
+  const QuantizeJob j{x, codes, scales, rule, qmax, 0, rotate, nullptr};
   return launch_quantize(&j, 1, BH, N, s);
 }
 
 cudaError_t launch_quantize_v(const void* v, int64_t BH, int64_t N, void* codes, void* scales, int rule,
                               double qmax, cudaStream_t s) {
-  const QuantizeJob j{v, codes, scales, rule, qmax, 1, 0};
+  const QuantizeJob j{v, codes, scales, rule, qmax, 1, 0, nullptr};
   return launch_quantize(&j, 1, BH, N, s);
 }
 

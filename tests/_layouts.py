@@ -59,3 +59,23 @@ def phat_values(codes: np.ndarray, scales: np.ndarray, e2m1_values: np.ndarray) 
     c = unpack_nibbles(np.asarray(codes, dtype=np.uint8))
     s = np.repeat(np.asarray(scales, dtype=np.int64), 32, axis=-1)
     return np.ldexp(e2m1_values[c], s - 127)
+
+
+def nv_tiles_logical(scales: np.ndarray, BH: int, N: int) -> np.ndarray:
+    """NVFP4 scales [BH*NT*1024] bytes (two atoms per tile, atom kk = blocks 4kk..4kk+3)
+    -> [BH, NT*128 rows, 8 blocks]."""
+    s = np.asarray(scales, dtype=np.uint8).reshape(BH, nt(N), 2, 512)
+    g = s[:, :, :, atom_index()]  # [BH, NT, 2, 128, 4]
+    g = np.transpose(g, (0, 1, 3, 2, 4)).reshape(BH, nt(N), 128, 8)
+    return g.reshape(BH, nt(N) * 128, 8)
+
+
+def nv_qk_scales_logical(scales: np.ndarray, BH: int, N: int) -> np.ndarray:
+    return nv_tiles_logical(scales, BH, N)[:, :N, :]
+
+
+def nv_v_scales_logical(scales: np.ndarray, BH: int, N: int) -> np.ndarray:
+    """-> [BH, 128 channels, ceil(N/16) token blocks]."""
+    t = nv_tiles_logical(scales, BH, N).reshape(BH, nt(N), 128, 8)  # rows = channels
+    g = np.transpose(t, (0, 2, 1, 3)).reshape(BH, 128, nt(N) * 8)
+    return g[:, :, : (N + 15) // 16]
