@@ -199,6 +199,25 @@ MXATTN_API mxattn_status mxattn_nvfp4_quantize_qk(const void* x, int64_t B, int6
                                                   void* codes, void* scales, float* amax, void* stream);
 MXATTN_API mxattn_status mxattn_nvfp4_quantize_v(const void* v, int64_t B, int64_t H, int64_t N, int64_t D,
                                                  void* codes, void* scales, float* amax, void* stream);
+/* The attention loop on NVFP4 operands, as the NVFP4 baseline: S from the
+ * tcgen05 kind::mxf4nvf4 (scale_vec::4X, UE4M3) product times
+ * 1/(e_tQ e_tK); P~ quantized per 16-key block with the E4M3 scale of its
+ * maximum / 6 and no tensor scale; O = (P^ V^ / e_tV) / l.
+ *   *_codes, *_scales, *_amax : from mxattn_nvfp4_quantize_qk (Q, K) and
+ *                               mxattn_nvfp4_quantize_v (V)
+ *   causal    : 0, or 1 with the query's own 16-token V block taken from the
+ *               bf16 rows (v_bf16 required). The tensor maximum behind e_t is
+ *               a statistic of the whole sequence: rows see future tokens
+ *               through it unless the maxima are fixed ahead of time.
+ *   placement : MXATTN_PLACE_DIRECT (l from P~, the baseline) or
+ *               MXATTN_PLACE_PNQ (l from P^)
+ *   out       : fp32 [B, H, N, 128] (device)
+ * Errors as for mxattn_forward. */
+MXATTN_API mxattn_status mxattn_nvfp4_forward(const void* q_codes, const void* q_scales, const float* q_amax,
+                                              const void* k_codes, const void* k_scales, const float* k_amax,
+                                              const void* v_codes, const void* v_scales, const float* v_amax,
+                                              const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D,
+                                              int causal, int placement, float* out, void* stream);
 
 /* Device workspace needed by mxattn_attention_host for [B, H, N, 128]. */
 MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);

@@ -21,7 +21,7 @@ __all__ = [
     "mxattn_forward_dump_phat", "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_workspace_bytes",
     "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
     "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes", "mxattn_nvfp4_quantize_qk",
-    "mxattn_nvfp4_quantize_v",
+    "mxattn_nvfp4_quantize_v", "mxattn_nvfp4_forward",
 ]
 
 D = 128
@@ -62,6 +62,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_nvfp4_scales_bytes.restype = SZ
         lib.mxattn_nvfp4_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
         lib.mxattn_nvfp4_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
+        lib.mxattn_nvfp4_forward.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P, P]
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
@@ -177,6 +178,18 @@ def mxattn_nvfp4_quantize_v(v: torch.Tensor, stream=None):
     _raise(load().mxattn_nvfp4_quantize_v(_ptr(v), B, H, N, Dx, _ptr(codes), _ptr(scales), _ptr(amax),
                                           _stream(stream)))
     return codes, scales, amax
+
+
+def mxattn_nvfp4_forward(q, k, v, v_bf16, B: int, H: int, N: int, causal: bool = False, placement: int = 1,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """NVFP4 forward; q, k, v are the (codes, scales, amax) triples of the NVFP4 quantizers.
+    placement 1 (direct, the baseline) or 0 (PNQ). Returns fp32 [B, H, N, 128]."""
+    dev = q[0].device
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
+    _raise(load().mxattn_nvfp4_forward(_ptr(q[0]), _ptr(q[1]), _ptr(q[2]), _ptr(k[0]), _ptr(k[1]), _ptr(k[2]),
+                                       _ptr(v[0]), _ptr(v[1]), _ptr(v[2]), _ptr(v_bf16), B, H, N, D, int(causal),
+                                       int(placement), _ptr(out), _stream(stream)))
+    return out
 
 
 def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,

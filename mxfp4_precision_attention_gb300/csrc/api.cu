@@ -112,7 +112,8 @@ mxattn_status check_quantizer_runtime() {
 mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                            const void* vs, const void* vb, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                            float* out, uint8_t* pc, uint8_t* ps, void* stream, int p_rule = kRuleUOS,
-                           int placement = kPlacePNQ, double p_qmax = 7.25) {
+                           int placement = kPlacePNQ, double p_qmax = 7.25, const float* q_amax = nullptr,
+                           const float* k_amax = nullptr, const float* v_amax = nullptr) {
   bool empty = false;
   MX_TRY(check_shape(B, H, N, D, &empty));
   if (empty) return MXATTN_OK;
@@ -133,11 +134,21 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
     MX_TRY(check_ptr(pc, "phat_codes"));
     MX_TRY(check_ptr(ps, "phat_scales"));
   }
+  const bool nv = q_amax != nullptr;
+  const size_t sfb = (nv ? 2 : 1) * sf_bytes(B, H, N);
   const Range ro = rng(out, f32_bytes(B, H, N));
-  const Range ins[] = {rng(qc, qk_codes(B, H, N)), rng(qs, sf_bytes(B, H, N)), rng(kc, qk_codes(B, H, N)),
-                       rng(ks, sf_bytes(B, H, N)),  rng(vc, v_codes(B, H, N)), rng(vs, sf_bytes(B, H, N))};
+  const Range ins[] = {rng(qc, qk_codes(B, H, N)), rng(qs, sfb), rng(kc, qk_codes(B, H, N)),
+                       rng(ks, sfb),  rng(vc, v_codes(B, H, N)), rng(vs, sfb)};
   for (const Range& r : ins)
     if (overlap(ro, r)) return fail(MXATTN_ERR_INVALID_ARG, "out overlaps an input buffer");
+  if (nv) {
+    for (const float* am : {q_amax, k_amax, v_amax}) {
+      if (am == nullptr || (reinterpret_cast<uintptr_t>(am) & 3u))
+        return fail(MXATTN_ERR_INVALID_ARG, "q_amax, k_amax and v_amax must be non-NULL, 4-byte aligned");
+      if (overlap(ro, rng(am, sizeof(float)))) return fail(MXATTN_ERR_INVALID_ARG, "out overlaps an amax");
+    }
+    if (causal == 2) return fail(MXATTN_ERR_INVALID_ARG, "the NVFP4 forward takes causal 0 or 1");
+  }
   if (causal && overlap(ro, rng(vb, bf16_bytes(B, H, N))))
     return fail(MXATTN_ERR_INVALID_ARG, "out overlaps v_bf16");
   Mxfp4FwdArgs a;
@@ -158,6 +169,9 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   a.p_rule = p_rule;
   a.placement = placement;
   a.p_qmax = p_qmax;
+  a.q_amax = q_amax;
+  a.k_amax = k_amax;
+  a.v_amax = v_amax;
   if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
   cudaError_t e = launch_mxfp4_forward(a, static_cast<cudaStream_t>(stream));
@@ -417,6 +431,17 @@ mxattn_status mxattn_forward_ex(const void* q_codes, const void* q_scales, const
   t_err[0] = '\0';
   return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
                       nullptr, nullptr, stream, p_rule, placement, p_qmax);
+}
+
+mxattn_status mxattn_nvfp4_forward(const void* q_codes, const void* q_scales, const float* q_amax,
+                                   const void* k_codes, const void* k_scales, const float* k_amax,
+                                   const void* v_codes, const void* v_scales, const float* v_amax, const void* v_bf16,
+                                   int64_t B, int64_t H, int64_t N, int64_t D, int causal, int placement, float* out,
+                                   void* stream) {
+  t_err[0] = '\0';
+  if (q_amax == nullptr) return fail(MXATTN_ERR_INVALID_ARG, "q_amax is NULL");
+  return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
+                      nullptr, nullptr, stream, kRuleUOS, placement, 7.25, q_amax, k_amax, v_amax);
 }
 
 mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,

@@ -58,14 +58,29 @@ constexpr uint32_t kOffQ = 0;                                 // 2 tiles
 constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;            // kKStages tiles
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;     // kVStages tiles (+ ones rows)
 constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]
-constexpr uint32_t kOffQSF = kOffP + 4 * kTileBytes;          // 2 atoms
-constexpr uint32_t kOffKSF = kOffQSF + 2 * kSfAtomBytes;      // kKStages atoms
-constexpr uint32_t kOffVSF = kOffKSF + kKStages * kSfAtomBytes;  // kVStages atoms
-constexpr uint32_t kOffOnesSF = kOffVSF + kVStages * kSfAtomBytes;  // constant atom (byte 127)
-constexpr uint32_t kOffBars = kOffOnesSF + kSfAtomBytes;
 constexpr int kNumBars = 40;
-constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+// Scale atoms, barriers and TMEM scale columns per operand format: MXFP4 has
+// one 512-byte atom per 128-row tile (4 blocks of 32 per row, both K halves in
+// one 32-bit TMEM word); NVFP4 has two (8 blocks of 16 per row, one word per
+// 64-wide MMA).
+template <bool kNv>
+struct Lay {
+  static constexpr uint32_t kSfTile = kNv ? 2 * kSfAtomBytes : kSfAtomBytes;  // scale bytes per tile
+  static constexpr uint32_t kOffQSF = kOffP + 4 * kTileBytes;                  // 2 tiles
+  static constexpr uint32_t kOffKSF = kOffQSF + 2 * kSfTile;                   // kKStages tiles
+  static constexpr uint32_t kOffVSF = kOffKSF + kKStages * kSfTile;            // kVStages tiles
+  static constexpr uint32_t kOffOnesSF = kOffVSF + kVStages * kSfTile;         // constant atom: scale 1
+  static constexpr uint32_t kOffBars = kOffOnesSF + kSfAtomBytes;
+  static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  // TMEM scale columns (S at 0, O_A and O_B at 128 .. 415)
+  //   MXFP4: Q [2 groups] x 4 | K [2 buffers] x 4 | P [2 groups][2 buffers] x 4 | V [2 buffers] x 8
+  //   NVFP4: each of those x 2 MMAs (K halves): 416 | 432 | 448 | 480, up to 512
+  static constexpr uint32_t kColSFQ = 416;
+  static constexpr uint32_t kColSFK = kNv ? 432 : 424;
+  static constexpr uint32_t kColSFP = kNv ? 448 : 432;
+  static constexpr uint32_t kColSFV = kNv ? 480 : 448;  // per buffer (x MMA): data atom, then the ones atom at +4
+};
 
 // mbarrier indices
 constexpr int kBarQFull = 0;
@@ -82,10 +97,6 @@ static_assert(kBarODone + 2 <= kNumBars, "barrier space");
 // TMEM columns
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;                 // O_g at kColO + g * kPvN (144 each)
-constexpr uint32_t kColSFQ = 416;               // [2 groups] x 4
-constexpr uint32_t kColSFK = 424;               // [2 buffers] x 4
-constexpr uint32_t kColSFP = 432;               // [2 groups][2 buffers] x 4
-constexpr uint32_t kColSFV = 448;               // [2 buffers] x 8 (upper 4: constant ones atom)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -112,6 +123,9 @@ struct Params {
   uint32_t diag_mant_thr;   // causal mode 2: scale rule of the re-quantized diagonal V block
   uint32_t diag_pow2_down;
   float score_scale_log2;  // log2(e) / sqrt(d)
+  const float* q_amax;     // NVFP4 kernels: the operands' tensor maxima (device)
+  const float* k_amax;
+  const float* v_amax;
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -128,6 +142,40 @@ __device__ __forceinline__ float max32(const float* v) {
   a[10] = fmaxf(v[30], v[31]);
   const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]), b2 = fmax3(a[6], a[7], a[8]);
   return fmaxf(fmax3(b0, b1, b2), fmaxf(a[9], a[10]));
+}
+
+__device__ __forceinline__ float max16(const float* v) {
+  const float a0 = fmax3(v[0], v[1], v[2]), a1 = fmax3(v[3], v[4], v[5]), a2 = fmax3(v[6], v[7], v[8]);
+  const float a3 = fmax3(v[9], v[10], v[11]), a4 = fmax3(v[12], v[13], v[14]);
+  return fmax3(fmax3(a0, a1, a2), fmax3(a3, a4, v[15]), v[15]);
+}
+
+constexpr float kSixth = 1.0f / 6.0f;  // binary32 nearest 1/6
+
+// E4M3 codes of two values >= 0 (round to nearest even, saturating at 448):
+// lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+// Values of two E4M3 codes (low byte -> .x), exact through f16.
+__device__ __forceinline__ float2 e4m3x2_values(uint32_t h) {
+  uint32_t hv;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hv) : "h"(static_cast<uint16_t>(h)));
+  return __half22float2(*reinterpret_cast<const __half2*>(&hv));
+}
+
+// 1 / e_t with e_t = fl32(2688 / amax), the tensor encode factor of an NVFP4 operand
+__device__ __forceinline__ float nv_decode(const float* amax) {
+  const float a = __ldg(amax);
+  return a > 0.0f ? __frcp_rn(__fdiv_rn(2688.0f, a)) : 1.0f;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float e2m1_decode(uint32_t nib) {
@@ -173,10 +221,15 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
 // floor of Eq. 11, TFS of Eq. 14, or the ceil rule with a swept Q_max of
 // section 5.5.1) and l may come from the unquantized P~
 // (direct placement, Eqs. 16-17) instead of P^ (PNQ, Eq. 47).
-template <bool kCausal, bool kDump, bool kVariant>
+template <bool kCausal, bool kDump, bool kVariant, bool kNv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  static_assert(!kNv || (kVariant && !kDump), "NVFP4 runs as a variant kernel without the P^ dump");
+  using L = Lay<kNv>;
+  constexpr uint32_t kOffQSF = L::kOffQSF, kOffKSF = L::kOffKSF, kOffVSF = L::kOffVSF, kOffOnesSF = L::kOffOnesSF;
+  constexpr uint32_t kOffBars = L::kOffBars, kOffMisc = L::kOffMisc, kSfTile = L::kSfTile;
+  constexpr uint32_t kColSFQ = L::kColSFQ, kColSFK = L::kColSFK, kColSFP = L::kColSFP, kColSFV = L::kColSFV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -231,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = t; i < kOnesRows * kD / 8; i += 256) ones[i] = 0x22222222u;
     }
     uint32_t* sf1 = reinterpret_cast<uint32_t*>(smem + kOffOnesSF);
-    for (int i = t; i < kSfAtomBytes / 4; i += 256) sf1[i] = 0x7F7F7F7Fu;
+    // scale 1: E8M0 byte 127, or E4M3 byte 0x38
+    for (int i = t; i < kSfAtomBytes / 4; i += 256) sf1[i] = kNv ? 0x38383838u : 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -246,12 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       const int ng = has_b ? 2 : 1;
-      mbar_arrive_expect_tx(bar(kBarQFull), ng * (kTileBytes + kSfAtomBytes));
+      mbar_arrive_expect_tx(bar(kBarQFull), ng * (kTileBytes + kSfTile));
       for (int g = 0; g < ng; g++) {
         const int qtg = g ? qtile1 : qtile0;
         tma_load_3d(sb + kOffQ + g * kTileBytes, &tm_q, bar(kBarQFull), 0, qtg * kTile, bh);
-        bulk_load(sb + kOffQSF + g * kSfAtomBytes,
-                  p.q_scales + (static_cast<int64_t>(bh) * p.NT + qtg) * kSfAtomBytes, kSfAtomBytes,
+        bulk_load(sb + kOffQSF + g * kSfTile, p.q_scales + (static_cast<int64_t>(bh) * p.NT + qtg) * kSfTile, kSfTile,
                   bar(kBarQFull));
       }
       int nk = 0, nv = 0;
@@ -261,10 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_error(p.status, 4, abort_flag);
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarKFull + ks), kTileBytes + kSfAtomBytes);
+        mbar_arrive_expect_tx(bar(kBarKFull + ks), kTileBytes + kSfTile);
         tma_load_3d(sb + kOffK + ks * kTileBytes, &tm_k, bar(kBarKFull + ks), 0, j * kTile, bh);
-        bulk_load(sb + kOffKSF + ks * kSfAtomBytes,
-                  p.k_scales + (static_cast<int64_t>(bh) * p.NT + j) * kSfAtomBytes, kSfAtomBytes,
+        bulk_load(sb + kOffKSF + ks * kSfTile, p.k_scales + (static_cast<int64_t>(bh) * p.NT + j) * kSfTile, kSfTile,
                   bar(kBarKFull + ks));
         nk++;
         const int vs = j % kVStages, vu = j / kVStages;
@@ -272,10 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_error(p.status, 4, abort_flag);
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarVFull + vs), kTileBytes + kSfAtomBytes);
+        mbar_arrive_expect_tx(bar(kBarVFull + vs), kTileBytes + kSfTile);
         tma_load_3d(sb + kOffV + vs * kVTileBytes, &tm_v, bar(kBarVFull + vs), j * (kTile / 2), 0, bh);
-        bulk_load(sb + kOffVSF + vs * kSfAtomBytes,
-                  p.v_scales + (static_cast<int64_t>(bh) * p.NT + j) * kSfAtomBytes, kSfAtomBytes,
+        bulk_load(sb + kOffVSF + vs * kSfTile, p.v_scales + (static_cast<int64_t>(bh) * p.NT + j) * kSfTile, kSfTile,
                   bar(kBarVFull + vs));
         nv++;
       }
@@ -288,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- QK issuer
     if (lane == 0) {
-      const uint32_t id0 = idesc_mxf4(128, kTile, 0, 0), id1 = idesc_mxf4(128, kTile, 2, 2);
+      const uint32_t id0 = kNv ? idesc_nvf4(128, kTile) : idesc_mxf4(128, kTile, 0, 0);
+      const uint32_t id1 = kNv ? idesc_nvf4(128, kTile) : idesc_mxf4(128, kTile, 2, 2);
       // operand descriptors computed once; a stage or buffer moves only the
       // start-address field (16-byte units), which cannot carry out of it here
       const uint64_t dq0 = smem_desc(sb + kOffQ, 16, 512, kSwizzle64B);
@@ -297,16 +349,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
       if (ok) {
         tc_fence_after();
-        tc_cp_sf(tmem + kColSFQ, smem_desc(sb + kOffQSF, 0, 128, kSwizzleNone));
-        if (has_b) tc_cp_sf(tmem + kColSFQ + 4, smem_desc(sb + kOffQSF + kSfAtomBytes, 0, 128, kSwizzleNone));
+        if constexpr (kNv) {
+          // tile g's atom kk (K half kk) -> columns kColSFQ + 8g + 4kk
+          for (int gg = 0; gg < (has_b ? 2 : 1); gg++)
+            for (int kk = 0; kk < 2; kk++)
+              tc_cp_sf(tmem + kColSFQ + 8 * gg + 4 * kk,
+                       smem_desc(sb + kOffQSF + gg * kSfTile + kk * kSfAtomBytes, 0, 128, kSwizzleNone));
+        } else {
+          tc_cp_sf(tmem + kColSFQ, smem_desc(sb + kOffQSF, 0, 128, kSwizzleNone));
+          if (has_b) tc_cp_sf(tmem + kColSFQ + 4, smem_desc(sb + kOffQSF + kSfAtomBytes, 0, 128, kSwizzleNone));
+        }
       }
       int n = 0;  // S productions so far
       for (int j = 0; ok && j < T; j++) {
         const int ks = j % kKStages;
         if (!mbar_wait(bar(kBarKFull + ks), (j / kKStages) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sfk = tmem + kColSFK + 4 * (j & 1);
-        tc_cp_sf(sfk, dsfk0 + ks * (kSfAtomBytes >> 4));
+        const uint32_t sfk = tmem + kColSFK + (kNv ? 8 : 4) * (j & 1);
+        tc_cp_sf(sfk, dsfk0 + ks * (kSfTile >> 4));
+        if constexpr (kNv) tc_cp_sf(sfk + 4, dsfk0 + ks * (kSfTile >> 4) + (kSfAtomBytes >> 4));
         const uint64_t dk = dk0 + ks * (kTileBytes >> 4);
         for (int g = 0; g < 2; g++) {
           if (j >= (g ? ntiles1 : ntiles0)) continue;
@@ -314,9 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n >= 1 && !mbar_wait(bar(kBarSEmpty), (n - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dq = dq0 + g * (kTileBytes >> 4);
-          const uint32_t sfq = tmem + kColSFQ + 4 * g;
-          mma_mxf4(tmem + kColS, dq, dk, id0, sfq, sfk, 0u);
-          mma_mxf4(tmem + kColS, dq + 2, dk + 2, id1, sfq, sfk, 1u);  // K step 1: +32 bytes
+          if constexpr (kNv) {
+            const uint32_t sfq = tmem + kColSFQ + 8 * g;
+            mma_nvf4(tmem + kColS, dq, dk, id0, sfq, sfk, 0u);
+            mma_nvf4(tmem + kColS, dq + 2, dk + 2, id1, sfq + 4, sfk + 4, 1u);  // K step 1: +32 bytes
+          } else {
+            const uint32_t sfq = tmem + kColSFQ + 4 * g;
+            mma_mxf4(tmem + kColS, dq, dk, id0, sfq, sfk, 0u);
+            mma_mxf4(tmem + kColS, dq + 2, dk + 2, id1, sfq, sfk, 1u);  // K step 1: +32 bytes
+          }
           if (!((p.debug_flags & kDebugNeverArriveS) && n == 0)) tc_commit(bar(kBarSFull + g));
           n++;
         }
@@ -328,19 +395,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2) {
     // --------------------------------------------------------- PV issuer
     if (lane == 0) {
-      const uint32_t id0 = idesc_mxf4(128, kPvN, 0, 0), id1 = idesc_mxf4(128, kPvN, 2, 2);
+      const uint32_t id0 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 0, 0);
+      const uint32_t id1 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 2, 2);
       const uint64_t dp0 = smem_desc(sb + kOffP, 16, 512, kSwizzle64B);
       const uint64_t dv0 = smem_desc(sb + kOffV, 16, 512, kSwizzle64B);
       const uint64_t dsfv0 = smem_desc(sb + kOffVSF, 0, 128, kSwizzleNone);
-      // scale atom of the ones rows, once into both V scale buffers
-      tc_cp_sf(tmem + kColSFV + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
-      tc_cp_sf(tmem + kColSFV + 12, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+      // scale atom of the ones rows, once into both V scale buffers (each K half for NVFP4)
+      if constexpr (kNv) {
+        for (int i = 0; i < 4; i++) tc_cp_sf(tmem + kColSFV + 8 * i + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+      } else {
+        tc_cp_sf(tmem + kColSFV + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+        tc_cp_sf(tmem + kColSFV + 12, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+      }
       bool ok = true;
       for (int j = 0; ok && j < T; j++) {
         const int vs = j % kVStages;
         if (!mbar_wait(bar(kBarVFull + vs), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
         const uint64_t dv = dv0 + vs * (kVTileBytes >> 4);
-        const uint32_t sfv = tmem + kColSFV + 8 * (j & 1);
+        const uint32_t sfv = tmem + kColSFV + (kNv ? 16 : 8) * (j & 1);
         bool sfv_loaded = false;
         for (int g = 0; g < 2; g++) {
           if (j >= (g ? ntiles1 : ntiles0)) continue;
@@ -349,14 +421,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!sfv_loaded) {
             // the previous user of this buffer (tile j-2) is complete: the softmax
             // threads waited for it before arriving on p_full
-            tc_cp_sf(sfv, dsfv0 + vs * (kSfAtomBytes >> 4));
+            tc_cp_sf(sfv, dsfv0 + vs * (kSfTile >> 4));
+            if constexpr (kNv) tc_cp_sf(sfv + 8, dsfv0 + vs * (kSfTile >> 4) + (kSfAtomBytes >> 4));
             sfv_loaded = true;
           }
           const uint64_t dp = dp0 + (2 * g + (j & 1)) * (kTileBytes >> 4);
-          const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
           const uint32_t od = tmem + kColO + g * kPvN;
-          mma_mxf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
-          mma_mxf4(od, dp + 2, dv + 2, id1, sfp, sfv, 1u);
+          if constexpr (kNv) {
+            const uint32_t sfp = tmem + kColSFP + 16 * g + 8 * (j & 1);
+            mma_nvf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
+            mma_nvf4(od, dp + 2, dv + 2, id1, sfp + 4, sfv + 8, 1u);
+          } else {
+            const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
+            mma_mxf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
+            mma_mxf4(od, dp + 2, dv + 2, id1, sfp, sfv, 1u);
+          }
           tc_commit(bar(kBarODone + g));
         }
         if (!ok) break;
@@ -374,12 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t qrow = static_cast<int64_t>(g ? qtile1 : qtile0) * kTile + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t ocol = kColO + g * kPvN;
-    const float C = p.score_scale_log2;
+    // NVFP4: S and O carry the tensor encode factors; undo them in C (Q, K) and in the epilogue (V)
+    const float C = kNv ? p.score_scale_log2 * nv_decode(p.q_amax) * nv_decode(p.k_amax) : p.score_scale_log2;
+    const float vdq = kNv ? nv_decode(p.v_amax) : 1.0f;
     const bool ragged = (N % kTile) != 0;
     float m_run = -INFINITY;
     bool my_abort = false;
     uint32_t diag_words[4] = {0u, 0u, 0u, 0u};  // causal: P^ codes of the query's own 32-key block
     uint32_t diag_sbyte = 127;
+    float diag_s = 0.0f;  // NVFP4: E4M3 scale value of the query's own 16-key block
     float l_direct = 0.0f;  // variant kernels, direct placement: l from P~ (Eq. 16)
     // all lanes poll; the outcome is made warp-uniform so tcgen05 .sync.aligned ops stay convergent
     auto wait_uniform = [&](int b, uint32_t parity) {
@@ -430,107 +512,188 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 128; i++) v[i] = (i < nvalid) ? v[i] : -INFINITY;
       }
-      float bm[4];
-#pragma unroll
-      for (int b = 0; b < 4; b++) bm[b] = max32(v + 32 * b);
-      const float m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
-      const float mc = m_new * C;
-
-      // The P^ buffer and TMEM scale columns of parity pb were last read by P^V^ of
-      // tile j-2; this thread saw that product complete in its o_done wait of tile j-1.
-      // P^ = Q*(exp(S/sqrt(d) - m_new)) per 32-key block with the UOS scale of the
-      // block maximum. Branch-free: a fully masked block has max -inf, all its
-      // exponentials are 0 and it takes the all-zero-block scale (byte 127).
-      uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
-      const int swz = (r >> 1) & 3;
-      const bool diag_tile = kCausal && j == Tg - 1;
-      uint8_t* dump = (kDump && qrow < N)
-                          ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
-                          : nullptr;
-      const float2 c2 = make_float2(C, C);
-      // UOS exponents of the four blocks, two at a time on the FMA pipe:
-      // e = ceil(max((bm - m_new)*C - log2 7.25, -127)). The block's offset
-      // bm - m_new is formed first, so the block holding the row maximum has
-      // log2 of its P~ maximum exactly 0 (this matters where a rule's
-      // boundary lies on an integer, as for the OCP floor). Adding kExpMagic
-      // (1.5*2^23 + 127) rounding toward +inf lands on kExpMagic + e exactly
-      // (unit spacing there), so the low byte of its bits is the E8M0 byte
-      // e + 127, and kExpMagic - t recovers -e exactly.
-      float qoff = kLog2Qmax;
-      if constexpr (kVariant)
-        qoff = p.p_rule == kRuleTFS ? kLog2Six
-               : p.p_rule == kRuleOCP ? 2.0f
-               : p.p_rule == kRuleCeilQ ? p.p_log2q
-                                         : kLog2Qmax;
-      const float2 nm2 = make_float2(-m_new, -m_new), nq2 = make_float2(-qoff, -qoff);
-      const float2 xe01 = __ffma2_rn(__fadd2_rn(make_float2(bm[0], bm[1]), nm2), c2, nq2);
-      const float2 xe23 = __ffma2_rn(__fadd2_rn(make_float2(bm[2], bm[3]), nm2), c2, nq2);
-      const float2 mg = make_float2(kExpMagic, kExpMagic);
-      float2 t01, t23;
-      if (kVariant && p.p_rule == kRuleOCP) {
-        // OCP: e = floor(log2 M) - 2, the same add rounding toward -inf
-        t01 = __fadd2_rd(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
-        t23 = __fadd2_rd(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
-      } else {
-        t01 = __fadd2_ru(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
-        t23 = __fadd2_ru(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
-      }
-      // -(mc + e), rounded once as mc + e would be
-      const float2 nmc = make_float2(-mc, -mc), neg1 = make_float2(-1.0f, -1.0f);
-      const float2 no01 = __fadd2_rn(__ffma2_rn(t01, neg1, mg), nmc);
-      const float2 no23 = __fadd2_rn(__ffma2_rn(t23, neg1, mg), nmc);
-      uint32_t sbytes = __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
-                                    __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
-      if (masked) {
-        // all-zero (fully masked) blocks take sigma = 1
-#pragma unroll
-        for (int b = 0; b < 4; b++)
-          if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
-      }
+      float m_new;
       float tile_ptilde = 0.0f;  // direct placement: sum of this row's P~ over the tile
+      if constexpr (kNv) {
+        // NVFP4 P~ (the comparison baseline): 16-key blocks, E4M3 scale of
+        // M/6 where M = 2^((bm - m_new) C) is the block's P~ maximum (exactly 1
+        // in the block of the row maximum), no further softmax-path scaling.
+        // The offset -log2(S) - m_new C goes into every element's 2^x, so y is
+        // P~ / S and its E2M1 code is the block's code.
+        float bm[8];
 #pragma unroll
-      for (int b = 0; b < 4; b++) {
-        const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
-        const float2 noff2 = make_float2(noff, noff);
-        uint32_t w[4];
-        float2 ysum = make_float2(0.0f, 0.0f);
+        for (int b = 0; b < 8; b++) bm[b] = max16(v + 16 * b);
+        m_new = fmax3(fmax3(m_run, bm[0], bm[1]), fmax3(bm[2], bm[3], bm[4]), fmax3(bm[5], bm[6], bm[7]));
+        const float mc = m_new * C;
+        uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
+        const int swz = (r >> 1) & 3;
+        const bool diag_tile = kCausal && j == Tg - 1;
+        const float2 c2 = make_float2(C, C);
+        // A block whose scale rounds to 0 (P~ max / 6 below 2^-10) has P^ = 0
+        // whatever its codes (the tensor core multiplies them by the zero
+        // scale): its y is P~ itself (divisor 1), so that l under direct
+        // placement still sums every P~.
+        uint32_t sw[2] = {0u, 0u};  // scale bytes of blocks 0-3 (first K half) and 4-7
+        float sv[8], sdiv[8], noff[8];
 #pragma unroll
-        for (int gq = 0; gq < 4; gq++) {
-          float y[8];
+        for (int b = 0; b < 8; b += 2) {
+          const float2 xm = __fmul2_rn(__fadd2_rn(make_float2(bm[b], bm[b + 1]), make_float2(-m_new, -m_new)), c2);
+          const float2 v6 = __fmul2_rn(make_float2(ex2_approx(xm.x), ex2_approx(xm.y)), make_float2(kSixth, kSixth));
+          const uint32_t h = e4m3x2(v6.x, v6.y);  // block b in the low byte
+          const float2 S = e4m3x2_values(h);
+          sv[b] = S.x;
+          sv[b + 1] = S.y;
+          sdiv[b] = S.x > 0.0f ? S.x : 1.0f;
+          sdiv[b + 1] = S.y > 0.0f ? S.y : 1.0f;
+          noff[b] = -lg2_approx(sdiv[b]) - mc;
+          noff[b + 1] = -lg2_approx(sdiv[b + 1]) - mc;
+          sw[b / 4] |= h << (8 * (b % 4));
+        }
 #pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
-            y[i] = ex2_approx(x.x);
-            y[i + 1] = ex2_approx(x.y);
-            if constexpr (kVariant) ysum = __fadd2_rn(ysum, make_float2(y[i], y[i + 1]));
+        for (int c = 0; c < 4; c++) {  // 32-key chunk c: blocks 2c and 2c+1
+          uint32_t w[4];
+#pragma unroll
+          for (int hb = 0; hb < 2; hb++) {
+            const int b = 2 * c + hb;
+            const float2 noff2 = make_float2(noff[b], noff[b]);
+            float2 ysum = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int gq = 0; gq < 2; gq++) {
+              float y[8];
+#pragma unroll
+              for (int i = 0; i < 8; i += 2) {
+                const float2 x = __ffma2_rn(make_float2(v[16 * b + 8 * gq + i], v[16 * b + 8 * gq + i + 1]), c2, noff2);
+                y[i] = ex2_approx(x.x);
+                y[i + 1] = ex2_approx(x.y);
+                ysum = __fadd2_rn(ysum, make_float2(y[i], y[i + 1]));
+              }
+              w[2 * hb + gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+            }
+            tile_ptilde = fmaf(ysum.x + ysum.y, sdiv[b], tile_ptilde);
           }
-          w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+          if (diag_tile && c == quad) {
+            // the query's own 16-key block (first or second half of the warp's
+            // 32 keys): its codes feed the bf16-V product, not the tensor core
+            const bool hi = lane >= 16;
+            diag_words[0] = hi ? 0u : w[0];
+            diag_words[1] = hi ? 0u : w[1];
+            diag_words[2] = hi ? w[2] : 0u;
+            diag_words[3] = hi ? w[3] : 0u;
+            w[0] = hi ? w[0] : 0u;
+            w[1] = hi ? w[1] : 0u;
+            w[2] = hi ? 0u : w[2];
+            w[3] = hi ? 0u : w[3];
+            diag_s = hi ? sv[2 * c + 1] : sv[2 * c];
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if constexpr (kVariant) {
-          // y = P~ / 2^e of the block; 2^e from the scale byte (byte 0 is 2^-127)
-          const uint32_t sb_b = (sbytes >> (8 * b)) & 0xFFu;
-          const float scale = sb_b ? __uint_as_float(sb_b << 23) : __uint_as_float(0x00400000u);
-          tile_ptilde = fmaf(ysum.x + ysum.y, scale, tile_ptilde);
+        // P^ scales: lane r, column base + r/32 of each K half's scale word
+        tmem_st1(tl + kColSFP + 16 * g + 8 * pb + quad, sw[0]);
+        tmem_st1(tl + kColSFP + 16 * g + 8 * pb + 4 + quad, sw[1]);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+      } else {
+        float bm[4];
+  #pragma unroll
+        for (int b = 0; b < 4; b++) bm[b] = max32(v + 32 * b);
+        m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+        const float mc = m_new * C;
+
+        // The P^ buffer and TMEM scale columns of parity pb were last read by P^V^ of
+        // tile j-2; this thread saw that product complete in its o_done wait of tile j-1.
+        // P^ = Q*(exp(S/sqrt(d) - m_new)) per 32-key block with the UOS scale of the
+        // block maximum. Branch-free: a fully masked block has max -inf, all its
+        // exponentials are 0 and it takes the all-zero-block scale (byte 127).
+        uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
+        const int swz = (r >> 1) & 3;
+        const bool diag_tile = kCausal && j == Tg - 1;
+        uint8_t* dump = (kDump && qrow < N)
+                            ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
+                            : nullptr;
+        const float2 c2 = make_float2(C, C);
+        // UOS exponents of the four blocks, two at a time on the FMA pipe:
+        // e = ceil(max((bm - m_new)*C - log2 7.25, -127)). The block's offset
+        // bm - m_new is formed first, so the block holding the row maximum has
+        // log2 of its P~ maximum exactly 0 (this matters where a rule's
+        // boundary lies on an integer, as for the OCP floor). Adding kExpMagic
+        // (1.5*2^23 + 127) rounding toward +inf lands on kExpMagic + e exactly
+        // (unit spacing there), so the low byte of its bits is the E8M0 byte
+        // e + 127, and kExpMagic - t recovers -e exactly.
+        float qoff = kLog2Qmax;
+        if constexpr (kVariant)
+          qoff = p.p_rule == kRuleTFS ? kLog2Six
+                 : p.p_rule == kRuleOCP ? 2.0f
+                 : p.p_rule == kRuleCeilQ ? p.p_log2q
+                                           : kLog2Qmax;
+        const float2 nm2 = make_float2(-m_new, -m_new), nq2 = make_float2(-qoff, -qoff);
+        const float2 xe01 = __ffma2_rn(__fadd2_rn(make_float2(bm[0], bm[1]), nm2), c2, nq2);
+        const float2 xe23 = __ffma2_rn(__fadd2_rn(make_float2(bm[2], bm[3]), nm2), c2, nq2);
+        const float2 mg = make_float2(kExpMagic, kExpMagic);
+        float2 t01, t23;
+        if (kVariant && p.p_rule == kRuleOCP) {
+          // OCP: e = floor(log2 M) - 2, the same add rounding toward -inf
+          t01 = __fadd2_rd(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
+          t23 = __fadd2_rd(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
+        } else {
+          t01 = __fadd2_ru(make_float2(fmaxf(xe01.x, -127.0f), fmaxf(xe01.y, -127.0f)), mg);
+          t23 = __fadd2_ru(make_float2(fmaxf(xe23.x, -127.0f), fmaxf(xe23.y, -127.0f)), mg);
         }
-        if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
-        if (diag_tile && b == quad) {
-          // the query's own 32-key block: keep its codes for the bf16-V product,
-          // drop it from the tensor-core operand
-#pragma unroll
+        // -(mc + e), rounded once as mc + e would be
+        const float2 nmc = make_float2(-mc, -mc), neg1 = make_float2(-1.0f, -1.0f);
+        const float2 no01 = __fadd2_rn(__ffma2_rn(t01, neg1, mg), nmc);
+        const float2 no23 = __fadd2_rn(__ffma2_rn(t23, neg1, mg), nmc);
+        uint32_t sbytes = __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
+                                      __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
+        if (masked) {
+          // all-zero (fully masked) blocks take sigma = 1
+  #pragma unroll
+          for (int b = 0; b < 4; b++)
+            if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
+        }
+  #pragma unroll
+        for (int b = 0; b < 4; b++) {
+          const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
+          const float2 noff2 = make_float2(noff, noff);
+          uint32_t w[4];
+          float2 ysum = make_float2(0.0f, 0.0f);
+  #pragma unroll
           for (int gq = 0; gq < 4; gq++) {
-            diag_words[gq] = w[gq];
-            w[gq] = 0u;
+            float y[8];
+  #pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
+              y[i] = ex2_approx(x.x);
+              y[i + 1] = ex2_approx(x.y);
+              if constexpr (kVariant) ysum = __fadd2_rn(ysum, make_float2(y[i], y[i + 1]));
+            }
+            w[gq] = pack_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
           }
-          diag_sbyte = (sbytes >> (8 * b)) & 0xFFu;
+          if constexpr (kVariant) {
+            // y = P~ / 2^e of the block; 2^e from the scale byte (byte 0 is 2^-127)
+            const uint32_t sb_b = (sbytes >> (8 * b)) & 0xFFu;
+            const float scale = sb_b ? __uint_as_float(sb_b << 23) : __uint_as_float(0x00400000u);
+            tile_ptilde = fmaf(ysum.x + ysum.y, scale, tile_ptilde);
+          }
+          if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (diag_tile && b == quad) {
+            // the query's own 32-key block: keep its codes for the bf16-V product,
+            // drop it from the tensor-core operand
+  #pragma unroll
+            for (int gq = 0; gq < 4; gq++) {
+              diag_words[gq] = w[gq];
+              w[gq] = 0u;
+            }
+            diag_sbyte = (sbytes >> (8 * b)) & 0xFFu;
+          }
+          *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (kDump && dump != nullptr)
+          *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
+        // P^ scales: lane r, column base + r/32 of this group's scale buffer
+        tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
+        fence_proxy_async_smem();
+        tmem_wait_st();
       }
-      if (kDump && dump != nullptr)
-        *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
-      // P^ scales: lane r, column base + r/32 of this group's scale buffer
-      tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
-      fence_proxy_async_smem();
-      tmem_wait_st();
       if constexpr (kVariant) l_direct = fmaf(ex2_approx((m_run - m_new) * C), l_direct, tile_ptilde);
       if (j >= 1) {
         // O_g is stable once P^V^ of tile j-1 completes; rescale by alpha if any row's max moved
@@ -592,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence1(lbits);
         float l = __uint_as_float(lbits);
-        const float dsc = __uint_as_float(diag_sbyte << 23);  // causal: 2^(byte-127) of the diagonal block
+        // causal: scale of the diagonal block (2^(byte-127), or the E4M3 value)
+        const float dsc = kNv ? diag_s : __uint_as_float(diag_sbyte << 23);
         const bool direct = kVariant && p.placement == kPlaceDirect;
         if constexpr (kCausal) {
           // the diagonal block's P^ is not in the tensor-core sum; direct
@@ -604,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (direct) l = l_direct;
         const float inv_l = 1.0f / l;
+        const float inv_lo = kNv ? inv_l * vdq : inv_l;  // O from the tensor cores carries V's encode factor
         float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
         if constexpr (!kCausal) {
 #pragma unroll 1
@@ -616,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
               for (int i = 0; i < 8; i++)
-                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                     __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_lo, __uint_as_float(o[4 * i + 1]) * inv_lo,
+                                     __uint_as_float(o[4 * i + 2]) * inv_lo, __uint_as_float(o[4 * i + 3]) * inv_lo);
             }
           }
         } else {
@@ -656,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence32(o);
             float acc[32];
 #pragma unroll
-            for (int i = 0; i < 32; i++) acc[i] = __uint_as_float(o[i]);
+            for (int i = 0; i < 32; i++) acc[i] = kNv ? __uint_as_float(o[i]) * vdq : __uint_as_float(o[i]);
             if (kVariant && p.causal == 2) {
               // Mode 2: the diagonal V block re-quantized per channel over keys
               // 0..lane (this row's prefix). Lane l reads key l's row; an
@@ -800,16 +965,25 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.p_log2q = static_cast<float>(std::log2(a.p_qmax));
   rule_threshold(a.p_rule, a.p_qmax, &p.diag_mant_thr, &p.diag_pow2_down);
   p.score_scale_log2 = kLog2e / 11.313708498984761f;  // log2(e) / sqrt(128)
+  p.q_amax = a.q_amax;
+  p.k_amax = a.k_amax;
+  p.v_amax = a.v_amax;
+  const bool nv = a.q_amax != nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static bool attr_set[64] = {false};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  constexpr uint32_t kSmemMx = Lay<false>::kSmemBytes, kSmemNv = Lay<true>::kSmemBytes;
   if (!attr_set[dev]) {
     for (auto fn : {mxfp4_fwd_kernel<false, false, false>, mxfp4_fwd_kernel<true, false, false>,
                     mxfp4_fwd_kernel<false, true, false>, mxfp4_fwd_kernel<true, true, false>,
                     mxfp4_fwd_kernel<false, false, true>, mxfp4_fwd_kernel<true, false, true>}) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMx);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<true, false, true, true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemNv);
       if (e != cudaSuccess) return e;
     }
     attr_set[dev] = true;
@@ -817,16 +991,20 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
   const bool dump = a.phat_codes != nullptr;
   const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ || a.causal == 2;
-  if (variant && dump) return cudaErrorNotSupported;  // the P^ dump covers UOS + PNQ only
-  if (variant) {
-    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+  if ((variant || nv) && dump) return cudaErrorNotSupported;  // the P^ dump covers MXFP4 UOS + PNQ only
+  if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
+  if (nv) {
+    if (a.causal) mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+  } else if (variant) {
+    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
   } else if (a.causal) {
-    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
   } else {
-    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
+    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
 }

@@ -63,6 +63,11 @@ struct Mxfp4FwdArgs {
   int p_rule;     // scale rule of the P~ blocks (kRule*)
   double p_qmax;  // Q_max of kRuleCeilQ
   int placement;  // kPlacePNQ: l from P^ (Eq. 47); kPlaceDirect: l from P~ (Eq. 16)
+  // NVFP4 operands (all three non-null, or all null for MXFP4): the tensors'
+  // max |x| from the NVFP4 quantizers; scales are then two E4M3 atoms per tile
+  const float* q_amax;
+  const float* k_amax;
+  const float* v_amax;
 };
 cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s);
 

@@ -176,6 +176,27 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32
          | (a_sf_id << 29);  // A scale-factor byte id
 }
 
+// Instruction descriptor, kind::mxf4nvf4 with scale_vec::4X (NVFP4: E2M1 x
+// E2M1, UE4M3 scales, 16-element blocks): all four bytes of the 32-bit TMEM
+// scale word belong to one MMA, so the scale-factor ids are 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7)           // A = E2M1
+         | (1u << 10)        // B = E2M1
+         | ((N >> 3) << 17)  // N
+         | (0u << 23)        // scale type UE4M3
+         | ((M >> 4) << 24);  // M
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(

@@ -6,6 +6,9 @@ P~ quantized, no smoothing, no softmax-path scaling), with the oracle's
 readings N1-N6:
   * quantizers: the tensor maximum, every E2M1 code and every E4M3 scale byte
     equal the oracle's (bit-exact; ragged N, special values);
+  * forward: max |O_gpu - O_oracle| <= 2e-3 * RMS(O_oracle) on every row of
+    small cases (ragged N, causal and not, direct and PNQ placement) and on
+    sampled rows at the Wan size; V == 1 gives O == 1 under PNQ.
 """
 import math
 
@@ -81,3 +84,99 @@ def test_nvfp4_quantizers_special_values(mx, orc):
     z = torch.zeros((1, 1, 200, 128), dtype=torch.bfloat16, device="cuda")
     c, s, a = mx.mxattn_nvfp4_quantize_qk(z)
     assert a.item() == 0.0 and not c.any() and not s.any()
+
+
+TOL_REL_RMS = 2e-3
+
+
+def _to_logical(mx, B, H, N, qt, kt, vt):
+    BH = B * H
+    qc = L.qk_codes_logical(qt[0].cpu().numpy(), BH, N)
+    qs = L.nv_qk_scales_logical(qt[1].cpu().numpy(), BH, N)
+    kc = L.qk_codes_logical(kt[0].cpu().numpy(), BH, N)
+    ks = L.nv_qk_scales_logical(kt[1].cpu().numpy(), BH, N)
+    vc = L.v_codes_logical(vt[0].cpu().numpy(), BH, N)
+    vs = L.nv_v_scales_logical(vt[1].cpu().numpy(), BH, N)
+    et = [float(np.float32(2688.0) / np.float32(t[2].item())) for t in (qt, kt, vt)]
+    return qc, qs, et[0], kc, ks, et[1], vc, vs, et[2]
+
+
+def _gpu_nv(mx, q, k, v, causal, placement):
+    B, H, N, _ = q.shape
+    qt, kt, vt = mx.mxattn_nvfp4_quantize_qk(q), mx.mxattn_nvfp4_quantize_qk(k), mx.mxattn_nvfp4_quantize_v(v)
+    out = mx.mxattn_nvfp4_forward(qt, kt, vt, v, B, H, N, causal=causal, placement=placement)
+    mx.mxattn_check()
+    return out, (qt, kt, vt)
+
+
+@pytest.mark.parametrize("placement", [1, 0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_nvfp4_forward_all_rows(mx, orc, causal, placement):
+    if causal:
+        q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=700, seed=19)
+    else:
+        q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=300)
+    B, H, N, _ = q.shape
+    out, _ = _gpu_nv(mx, q, k, v, causal, placement)
+    g = out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
+    qb, kb, vb = (W.as_u16(t).reshape(B * H, N, 128) for t in (q, k, v))
+    oqc, oqs, oqe = orc.nvfp4_quantize_qk(qb)
+    okc, oks, oke = orc.nvfp4_quantize_qk(kb)
+    ovc, ovs, ove = orc.nvfp4_quantize_v(vb)
+    rows = np.array([[b, i] for b in range(B * H) for i in range(N)], dtype=np.int64)
+    ref = orc.forward_nvfp4(oqc, oqs, oqe, okc, oks, oke, ovc, ovs, ove, rows, vraw_u16=vb, causal=causal,
+                            placement=placement)["out"].reshape(B * H, N, 128)
+    err = np.abs(g - ref).max()
+    rms = math.sqrt(np.mean(ref ** 2))
+    print(f"nvfp4 causal={causal} placement={placement}: max|err| {err:.3e}, RMS {rms:.3e}, ratio {err / rms:.3e}")
+    assert err <= TOL_REL_RMS * rms
+
+
+def test_nvfp4_forward_v_ones_pnq(mx):
+    q, k, _ = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=600, seed=23)
+    v = torch.ones_like(q)
+    for causal in (False, True):
+        pnq, _ = _gpu_nv(mx, q, k, v, causal, 0)
+        assert (pnq - 1.0).abs().max().item() <= 1e-5
+        direct, _ = _gpu_nv(mx, q, k, v, causal, 1)
+        assert (direct - 1.0).abs().max().item() > 1e-3
+
+
+@pytest.mark.parametrize("name,nrows", [("wan_32760", 48), ("causal_lm_8192", 64)])
+def test_nvfp4_forward_full_size_sampled(mx, orc, name, nrows):
+    """At the benchmark sizes: the oracle's loop on the GPU-quantized operands (the quantizers are pinned
+    bit-exact above; the tensor maxima are checked against torch here), on sampled rows."""
+    w = W.WORKLOADS[name]
+    q, k, v = W.generate(w, device="cuda")
+    out, (qt, kt, vt) = _gpu_nv(mx, q, k, v, w.causal, 1)
+    for t, x in ((qt, q), (kt, k), (vt, v)):
+        assert t[2].item() == x.abs().max().float().item()
+    BH, N = w.B * w.H, w.N
+    rng = np.random.default_rng(11)
+    heads = sorted(set([0, BH - 1, int(rng.integers(0, BH))]))
+    per = max(1, nrows // len(heads))
+    rows = []
+    for h in heads:
+        rows += [[h, int(i)] for i in rng.integers(0, N, per)]
+        rows += [[h, N - 1], [h, (N - 1) // 128 * 128]]
+    rows = np.array(rows, dtype=np.int64)
+    g = out.reshape(BH * N, 128).index_select(0, torch.tensor(rows[:, 0] * N + rows[:, 1], device="cuda"))
+    g = g.cpu().numpy().astype(np.float64)
+    # the listed heads only, in the oracle's logical layouts
+    idx = torch.tensor(heads, device="cuda")
+    sub = lambda t, per_head: t.reshape(BH, -1).index_select(0, idx).reshape(-1)
+    nh = len(heads)
+    qt_s = (sub(qt[0], 1), sub(qt[1], 1), qt[2])
+    kt_s = (sub(kt[0], 1), sub(kt[1], 1), kt[2])
+    vt_s = (sub(vt[0], 1), sub(vt[1], 1), vt[2])
+    ops = _to_logical(mx, 1, nh, N, qt_s, kt_s, vt_s)
+    vraw = W.as_u16(v.reshape(BH, N, 128).index_select(0, idx))
+    remap = {h: i for i, h in enumerate(heads)}
+    rr = np.array([[remap[int(b)], int(i)] for b, i in rows], dtype=np.int64)
+    ref = orc.forward_nvfp4(*ops, rr, vraw_u16=vraw, causal=w.causal, placement=1)["out"]
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    err = np.abs(g - ref).max()
+    rms = math.sqrt(np.mean(ref ** 2))
+    print(f"{name} nvfp4 sampled: max|err| {err:.3e}, ratio {err / rms:.3e}")
+    assert err <= TOL_REL_RMS * rms
