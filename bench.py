@@ -341,6 +341,32 @@ def run_ours(args, w):
         except Exception as ex:  # no fused backend for this GPU / torch build
             bf16_path["library_sdpa"] = {"unavailable": str(ex)[:200]}
 
+    # the NVFP4 comparison path on the same inputs (not part of the step): its
+    # quantizers (amax pass + tiles, per tensor) and the kind::mxf4nvf4 forward
+    nvfp4_path = None
+    if not args.no_nvfp4:
+        with torch.cuda.stream(stream):
+            n_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for rep in range(3):
+                if rep == 2: n_ev[0].record(stream)
+                qt = mx.mxattn_nvfp4_quantize_qk(q, stream=stream)
+                kt = mx.mxattn_nvfp4_quantize_qk(k, stream=stream)
+                vt = mx.mxattn_nvfp4_quantize_v(v, stream=stream)
+                if rep == 2: n_ev[1].record(stream)
+            for rep in range(5):
+                if rep == 2: n_ev[2].record(stream)
+                mx.mxattn_nvfp4_forward(qt, kt, vt, v, B, H, N, causal=w.causal, placement=1, out=out, stream=stream)
+            n_ev[3].record(stream)
+        torch.cuda.synchronize()
+        mx.mxattn_check(stream)
+        nq_ms = n_ev[0].elapsed_time(n_ev[1])
+        nf_ms = n_ev[2].elapsed_time(n_ev[3]) / 3
+        nt = flops / (nf_ms * 1e-3) / 1e12
+        nvfp4_path = {"kernel": "mxfp4_fwd_kernel NVFP4 instantiation (tcgen05 kind::mxf4nvf4 scale_vec::4X, UE4M3)",
+                      "placement": "direct (the baseline)", "forward_ms": nf_ms, "tflops": nt,
+                      "frac_of_fp4_peak": nt / fp4_peak, "quantize_ms": nq_ms, "mxfp4_speedup": nf_ms / fwd_ms}
+        del qt, kt, vt
+
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
     if not args.no_e2e:
@@ -396,6 +422,7 @@ def run_ours(args, w):
                           "single_calls": single},
             "gpu_launches": 2 * args.steps,
             "bf16_path": bf16_path,
+            "nvfp4_path": nvfp4_path,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -614,6 +641,19 @@ def run_accuracy(args):
                                           placement=placement)[..., 0]
                 res[name]["rowsum_mean"] = rs.mean().item()
                 res[name]["rowsum_min"] = rs.min().item()
+        # the NVFP4 baseline (section 5.2: direct l) and NVFP4 with PNQ
+        qt, kt, vt = mx.mxattn_nvfp4_quantize_qk(q), mx.mxattn_nvfp4_quantize_qk(k), mx.mxattn_nvfp4_quantize_v(v)
+        for label, placement in (("NVFP4 (direct l, the baseline)", 1), ("NVFP4 + PNQ", 0)):
+            out = mx.mxattn_nvfp4_forward(qt, kt, vt, v, B, H, N, causal=w.causal, placement=placement)
+            mx.mxattn_check()
+            res[label] = score(out)
+            if placement == 1:
+                ones = torch.ones_like(v)
+                ot = mx.mxattn_nvfp4_quantize_v(ones)
+                rs = mx.mxattn_nvfp4_forward(qt, kt, ot, ones, B, H, N, causal=w.causal, placement=1)[..., 0]
+                res[label]["rowsum_mean"] = rs.mean().item()
+                res[label]["rowsum_min"] = rs.min().item()
+        del qt, kt, vt
         res["bf16 path"] = score(mx.mxattn_forward_bf16(q, k, v, causal=w.causal))
         mx.mxattn_check()
         table[wname] = {"rows": len(rows), "results": res}
@@ -638,6 +678,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison-path timing")
+    ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 comparison-path timing")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--accuracy", action="store_true",
