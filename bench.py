@@ -143,6 +143,30 @@ def _dist():
     return world, rank, local
 
 
+def rank_seed(w, rank: int) -> int:
+    """Seed of rank `rank`'s replica: every rank runs the whole workload on its own inputs."""
+    return w.seed + rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The maximum of `x` over all ranks of the default process group (x itself
+    without one). `device` is where the collective's tensor lives: the GPU for
+    NCCL, the CPU for gloo."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flops_per_step: float, steps: int, seconds: float) -> float:
+    """Whole-job TFLOPS: every rank's steps over the slowest rank's time."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 def cpu_oracle_sample(w, budget_rows: int, seed: int = 0):
     """Time the oracle on a bounded sample of workload `w`: per sampled head, its
     K and V quantized in full plus up to N query rows through the forward, over
@@ -229,7 +253,7 @@ def run_ours(args, w):
     hbm, bf16, bf16_sus, peak_src = _peaks()
     fp4_peak = bf16 * FP4_OVER_BF16_NOMINAL
     B, H, N = w.B, w.H, w.N
-    q, k, v = W.generate(w, device="cuda", seed=w.seed + rank)
+    q, k, v = W.generate(w, device="cuda", seed=rank_seed(w, rank))
     qcn, qsn = mx.qk_layout_sizes(B, H, N)
     vcn, vsn = mx.v_layout_sizes(B, H, N)
     dev = q.device
@@ -273,18 +297,13 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     clk = clocks.stop()
     mx.mxattn_check(stream)
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-        dist.barrier()
+        torch.distributed.barrier()
     qkv_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n_events))
     fwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(n_events))
     flops = w.flops
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_value(world, flops, args.steps, total_ms * 1e-3)
     fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
     e = B * H * N * 128
     qkv_bytes = 2 * (e * 2 + qcn + qsn) + e * 2 + vcn + vsn
@@ -382,14 +401,8 @@ def run_ours(args, w):
         t0 = time.perf_counter()
         for _ in range(steps_e2e):
             mx.mxattn_attention_host(qh, kh, vh, w.causal, outh, ws, stream=stream)
-        dt = time.perf_counter() - t0
-        if world > 1:
-            import torch.distributed as dist
-
-            tt = torch.tensor([dt], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            dt = float(tt.item())
-        e2e = {"value": world * flops * steps_e2e / dt / 1e12, "unit": UNIT,
+        dt = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": job_value(world, flops, steps_e2e, dt), "unit": UNIT,
                "h2d_bytes_per_step": 3 * e * 2, "d2h_bytes_per_step": e * 4, "steps": steps_e2e,
                "api": "mxattn_attention_host (pinned host buffers, copies inside the timed region)"}
 
