@@ -218,6 +218,17 @@ MXATTN_API mxattn_status mxattn_nvfp4_forward(const void* q_codes, const void* q
                                               const void* v_codes, const void* v_scales, const float* v_amax,
                                               const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D,
                                               int causal, int placement, float* out, void* stream);
+/* Diagnostic variant of mxattn_nvfp4_forward that also writes every P^ tile,
+ * as mxattn_forward_dump_phat does: phat_codes [B*H][N][ceil(N/128)*64]
+ * (E2M1 codes, key 2i of a tile in the low nibble of byte i) and
+ * phat_scales [B*H][N][ceil(N/128)*8] (the E4M3 byte of each 16-key block). */
+MXATTN_API mxattn_status mxattn_nvfp4_forward_dump_phat(const void* q_codes, const void* q_scales,
+                                                        const float* q_amax, const void* k_codes,
+                                                        const void* k_scales, const float* k_amax,
+                                                        const void* v_codes, const void* v_scales,
+                                                        const float* v_amax, const void* v_bf16, int64_t B, int64_t H,
+                                                        int64_t N, int64_t D, int causal, int placement, float* out,
+                                                        uint8_t* phat_codes, uint8_t* phat_scales, void* stream);
 
 /* Device workspace needed by mxattn_attention_host for [B, H, N, 128]. */
 MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);

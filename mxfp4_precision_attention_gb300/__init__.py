@@ -22,6 +22,7 @@ __all__ = [
     "mxattn_check", "mxattn_set_debug_flags", "mxattn_attention", "qk_layout_sizes", "v_layout_sizes",
     "mxattn_attention_noalloc", "mxattn_attention_noalloc_max_scratch_bytes", "mxattn_nvfp4_quantize_qk",
     "mxattn_nvfp4_quantize_v", "mxattn_nvfp4_forward",
+    "mxattn_nvfp4_forward_dump_phat",
 ]
 
 D = 128
@@ -63,6 +64,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_nvfp4_quantize_qk.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
         lib.mxattn_nvfp4_quantize_v.argtypes = [P, I64, I64, I64, I64, P, P, P, P]
         lib.mxattn_nvfp4_forward.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P, P]
+        lib.mxattn_nvfp4_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, P, P,
+                                                       P, P]
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
@@ -190,6 +193,22 @@ def mxattn_nvfp4_forward(q, k, v, v_bf16, B: int, H: int, N: int, causal: bool =
                                        _ptr(v[0]), _ptr(v[1]), _ptr(v[2]), _ptr(v_bf16), B, H, N, D, int(causal),
                                        int(placement), _ptr(out), _stream(stream)))
     return out
+
+
+def mxattn_nvfp4_forward_dump_phat(q, k, v, v_bf16, B: int, H: int, N: int, causal: bool = False,
+                                   placement: int = 1, stream=None):
+    """mxattn_nvfp4_forward plus every P^ tile: returns (out, phat_codes [B*H, N, NT*64],
+    phat_scales [B*H, N, NT*8])."""
+    dev = q[0].device
+    nt = (N + 127) // 128
+    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+    pc = torch.zeros((B * H, N, nt * 64), dtype=torch.uint8, device=dev)
+    ps = torch.zeros((B * H, N, nt * 8), dtype=torch.uint8, device=dev)
+    _raise(load().mxattn_nvfp4_forward_dump_phat(_ptr(q[0]), _ptr(q[1]), _ptr(q[2]), _ptr(k[0]), _ptr(k[1]),
+                                                 _ptr(k[2]), _ptr(v[0]), _ptr(v[1]), _ptr(v[2]), _ptr(v_bf16), B, H,
+                                                 N, D, int(causal), int(placement), _ptr(out), _ptr(pc), _ptr(ps),
+                                                 _stream(stream)))
+    return out, pc, ps
 
 
 def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,

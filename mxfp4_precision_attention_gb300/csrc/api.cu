@@ -444,6 +444,19 @@ mxattn_status mxattn_nvfp4_forward(const void* q_codes, const void* q_scales, co
                       nullptr, nullptr, stream, kRuleUOS, placement, 7.25, q_amax, k_amax, v_amax);
 }
 
+mxattn_status mxattn_nvfp4_forward_dump_phat(const void* q_codes, const void* q_scales, const float* q_amax,
+                                             const void* k_codes, const void* k_scales, const float* k_amax,
+                                             const void* v_codes, const void* v_scales, const float* v_amax,
+                                             const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D,
+                                             int causal, int placement, float* out, uint8_t* phat_codes,
+                                             uint8_t* phat_scales, void* stream) {
+  t_err[0] = '\0';
+  if (q_amax == nullptr) return fail(MXATTN_ERR_INVALID_ARG, "q_amax is NULL");
+  if (phat_codes == nullptr || phat_scales == nullptr) return fail(MXATTN_ERR_INVALID_ARG, "phat dump needs both buffers");
+  return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
+                      phat_codes, phat_scales, stream, kRuleUOS, placement, 7.25, q_amax, k_amax, v_amax);
+}
+
 mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
                                   int64_t D, int causal, float* out, void* stream) {
   t_err[0] = '\0';

@@ -225,7 +225,7 @@ template <bool kCausal, bool kDump, bool kVariant, bool kNv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  static_assert(!kNv || (kVariant && !kDump), "NVFP4 runs as a variant kernel without the P^ dump");
+  static_assert(!kNv || kVariant, "NVFP4 runs as a variant kernel");
   using L = Lay<kNv>;
   constexpr uint32_t kOffQSF = L::kOffQSF, kOffKSF = L::kOffKSF, kOffVSF = L::kOffVSF, kOffOnesSF = L::kOffOnesSF;
   constexpr uint32_t kOffBars = L::kOffBars, kOffMisc = L::kOffMisc, kSfTile = L::kSfTile;
@@ -529,6 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int swz = (r >> 1) & 3;
         const bool diag_tile = kCausal && j == Tg - 1;
         const float2 c2 = make_float2(C, C);
+        uint8_t* dump = (kDump && qrow < N)
+                            ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
+                            : nullptr;
         // A block whose scale rounds to 0 (P~ max / 6 below 2^-10) has P^ = 0
         // whatever its codes (the tensor core multiplies them by the zero
         // scale): its y is P~ itself (divisor 1), so that l under direct
@@ -571,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tile_ptilde = fmaf(ysum.x + ysum.y, sdiv[b], tile_ptilde);
           }
+          if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
           if (diag_tile && c == quad) {
             // the query's own 16-key block (first or second half of the warp's
             // 32 keys): its codes feed the bf16-V product, not the tensor core
@@ -587,6 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        if (kDump && dump != nullptr)
+          *reinterpret_cast<uint2*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 8) =
+              make_uint2(sw[0], sw[1]);
         // P^ scales: lane r, column base + r/32 of each K half's scale word
         tmem_st1(tl + kColSFP + 16 * g + 8 * pb + quad, sw[0]);
         tmem_st1(tl + kColSFP + 16 * g + 8 * pb + 4 + quad, sw[1]);
@@ -982,7 +989,8 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMx);
       if (e != cudaSuccess) return e;
     }
-    for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<true, false, true, true>}) {
+    for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<true, false, true, true>,
+                    mxfp4_fwd_kernel<false, true, true, true>, mxfp4_fwd_kernel<true, true, true, true>}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemNv);
       if (e != cudaSuccess) return e;
     }
@@ -991,11 +999,16 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
   const bool dump = a.phat_codes != nullptr;
   const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ || a.causal == 2;
-  if ((variant || nv) && dump) return cudaErrorNotSupported;  // the P^ dump covers MXFP4 UOS + PNQ only
+  if (!nv && variant && dump) return cudaErrorNotSupported;  // the MXFP4 P^ dump covers UOS + PNQ only
   if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
   if (nv) {
-    if (a.causal) mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+    if (a.causal) {
+      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+    } else {
+      if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+      else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+    }
   } else if (variant) {
     if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
     else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);

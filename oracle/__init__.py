@@ -97,7 +97,7 @@ def _load():
             lib.orc_nvfp4_quantize_v.argtypes = [P, I64, I64, P, P, P]
             F32 = ctypes.c_float
             lib.orc_forward_nvfp4.argtypes = [P, P, F32, P, P, F32, P, P, F32, P, I64, I64, I, I, I, P, I64, P, P, P,
-                                              P]
+                                              P, P]
             lib.orc_forward_nvfp4.restype = I
             lib.orc_num_threads.restype = I
             _lib = lib
@@ -321,11 +321,12 @@ def nvfp4_quantize_v(v_u16: np.ndarray):
 
 
 def forward_nvfp4(qc, qs, q_et, kc, ks, k_et, vc, vs, v_et, rows, *, vraw_u16=None, causal=False,
-                  placement=DIRECT, quant_p=True, want_phat=False):
+                  placement=DIRECT, quant_p=True, want_phat=False, phat_in=None):
     """The attention loop on NVFP4 operands (logical layouts as returned above).
 
     P~ is quantized as NVFP4 (16-key blocks, e_t = 1). ``placement``: DIRECT
-    (l from P~, the baseline's reading) or PNQ. Returns dict as :func:`forward`."""
+    (l from P~, the baseline's reading) or PNQ. ``phat_in`` ``[R, ntiles*128]``:
+    replay those P^ values instead of computing them. Returns dict as :func:`forward`."""
     lib = _load()
     qc, qs, kc, ks, vc, vs = (_c(a, np.uint8) for a in (qc, qs, kc, ks, vc, vs))
     BH, N, _ = qc.shape
@@ -339,9 +340,12 @@ def forward_nvfp4(qc, qs, q_et, kc, ks, k_et, vc, vs, v_et, rows, *, vraw_u16=No
     ell = np.empty(R)
     phat = np.zeros((R, ntiles * BC)) if want_phat else None
     mhist = np.full((R, ntiles), np.nan) if want_phat else None
+    if phat_in is not None:
+        phat_in = _c(phat_in, np.float64).reshape(R, ntiles * BC)
     rc = lib.orc_forward_nvfp4(_p(qc), _p(qs), float(q_et), _p(kc), _p(ks), float(k_et), _p(vc), _p(vs),
                                float(v_et), _p(vr), BH, N, int(bool(causal)), int(placement), int(quant_p),
-                               _p(rows), R, _p(out), _p(ell), _p(phat), _p(mhist))
+                               _p(rows), R, _p(out), _p(ell), _p(phat), _p(mhist),
+                               _p(phat_in))
     if rc != 0:
         raise RuntimeError(f"orc_forward_nvfp4 failed with code {rc}")
     res = {"out": out, "ell": ell}

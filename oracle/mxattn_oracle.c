@@ -333,6 +333,7 @@ typedef struct {
   int bc;
   double p_q;
   int nv; /* 1: P~ quantized as NVFP4 (16-key blocks, E4M3 scale of M/6, N1-N5) */
+  const double* phat_in; /* replay: this row's P^ per tile (ntiles*bc) given, not computed */
 } orc_opts;
 
 static void online_softmax_row(const double* q, const double* K, const double* V, const double* Vraw,
@@ -387,7 +388,10 @@ static void online_softmax_row(const double* q, const double* K, const double* V
     /* Eq. 44: P^ = Q*(P~), 32-key blocks counted from key 0 (16 for NVFP4) */
     const int pblk = op->nv ? 16 : ORC_BLOCK;
     for (int b0 = 0; b0 < bc; b0 += pblk) {
-      if (op->quant_p && op->nv) {
+      if (op->phat_in) {
+        /* replay: the given P^ (a kernel's dumped codes and scales) on the valid keys */
+        for (int t = 0; t < pblk; t++) Ph[b0 + t] = valid[b0 + t] ? op->phat_in[j * bc + b0 + t] : 0.0;
+      } else if (op->quant_p && op->nv) {
         /* N2, N4 with e_t = 1, in float64: S = E4M3(fl(M / 6)), code = E2M1(P~ / S) */
         double M = 0.0;
         for (int t = 0; t < 16; t++)
@@ -442,7 +446,7 @@ void orc_online_softmax(const double* q_rows, const int64_t* row_tok, int64_t nr
                         const double* V, const double* Vraw, int64_t N, int causal, int quant_p,
                         int placement, int p_rule, double p_q, int bc, double* out, double* ell, double* phat,
                         double* mhist) {
-  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0, NULL};
   const int64_t ntiles = (N + bc - 1) / bc;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; r++) {
@@ -466,7 +470,7 @@ int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const u
   if (bc <= 0 || bc % ORC_BLOCK != 0) return 1;
   const int64_t nblk = (N + ORC_BLOCK - 1) / ORC_BLOCK;
   const int64_t ntiles = (N + bc - 1) / bc;
-  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0};
+  orc_opts op = {causal, quant_p, placement, p_rule, bc, p_q, 0, NULL};
   double* K = (double*)malloc(sizeof(double) * N * ORC_D);
   double* V = (double*)malloc(sizeof(double) * N * ORC_D);
   double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);
@@ -512,16 +516,18 @@ int orc_forward(const uint8_t* qc, const uint8_t* qs, const uint8_t* kc, const u
  * The same loop with NVFP4 operands: qc, kc, vc [BH][N][128] codes; qs, ks
  * [BH][N][8] E4M3 bytes; vs [BH][128][ceil(N/16)]; q_et, k_et, v_et the
  * tensors' encode factors. causal 0 or 1 (the own 16-token V block on bf16).
- * P~ is NVFP4-quantized when quant_p (N2, N4 with e_t = 1).                  */
+ * P~ is NVFP4-quantized when quant_p (N2, N4 with e_t = 1). phat_in (or NULL):
+ * replay mode, row r's P^ for every tile given ([nrows][ntiles*128]), so a
+ * kernel's own P^ decisions can be replayed through the float64 loop.      */
 int orc_forward_nvfp4(const uint8_t* qc, const uint8_t* qs, float q_et, const uint8_t* kc, const uint8_t* ks,
                       float k_et, const uint8_t* vc, const uint8_t* vs, float v_et, const uint16_t* vraw, int64_t BH,
                       int64_t N, int causal, int placement, int quant_p, const int64_t* rows, int64_t nrows,
-                      double* out, double* ell, double* phat, double* mhist) {
+                      double* out, double* ell, double* phat, double* mhist, const double* phat_in) {
   if (causal != 0 && causal != 1) return 1;
   const int bc = 128;
   const int64_t nblk = (N + 15) / 16;
   const int64_t ntiles = (N + bc - 1) / bc;
-  orc_opts op = {causal, quant_p, placement, 0, bc, 7.25, 1};
+  const orc_opts op0 = {causal, quant_p, placement, 0, bc, 7.25, 1, NULL};
   double* K = (double*)malloc(sizeof(double) * N * ORC_D);
   double* V = (double*)malloc(sizeof(double) * N * ORC_D);
   double* Vr = (double*)malloc(sizeof(double) * N * ORC_D);
@@ -553,6 +559,8 @@ int orc_forward_nvfp4(const uint8_t* qc, const uint8_t* qs, float q_et, const ui
         const int64_t e = (bh * N + i) * ORC_D + c;
         q[c] = nv_dq(qc[e], qs[(bh * N + i) * 8 + c / 16], q_et);
       }
+      orc_opts op = op0;
+      op.phat_in = phat_in ? phat_in + r * ntiles * bc : NULL;
       online_softmax_row(q, K, V, Vr, N, i, &op, out + r * ORC_D, ell + r,
                          phat ? phat + r * ntiles * bc : NULL, mhist ? mhist + r * ntiles : NULL);
     }

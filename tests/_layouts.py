@@ -79,3 +79,11 @@ def nv_v_scales_logical(scales: np.ndarray, BH: int, N: int) -> np.ndarray:
     t = nv_tiles_logical(scales, BH, N).reshape(BH, nt(N), 128, 8)  # rows = channels
     g = np.transpose(t, (0, 2, 1, 3)).reshape(BH, 128, nt(N) * 8)
     return g[:, :, : (N + 15) // 16]
+
+
+def nv_phat_values(codes: np.ndarray, scales: np.ndarray, e2m1_values: np.ndarray,
+                   e4m3_values: np.ndarray) -> np.ndarray:
+    """Dumped NVFP4 P^ tiles ([R, NT*64] codes, [R, NT*8] E4M3 scales) -> dequantized [R, NT*128]."""
+    c = unpack_nibbles(np.asarray(codes, dtype=np.uint8))
+    s = np.repeat(e4m3_values[np.asarray(scales, dtype=np.int64)], 16, axis=-1)
+    return e2m1_values[c] * s

@@ -75,7 +75,7 @@ def _flip_rate(orc, pc, ps, ora_phat, rows, N, causal):
     pcn, psn = pc.cpu().numpy(), ps.cpu().numpy()
     gp = L.phat_values(pcn[rows[:, 0], rows[:, 1]], psn[rows[:, 0], rows[:, 1]], vals)
     keys = np.arange(gp.shape[1])[None, :]
-    valid = keys < N
+    valid = np.broadcast_to(keys < N, gp.shape)
     if causal:
         valid = valid & (keys <= rows[:, 1:2])
     diff = (gp != ora_phat) & valid
@@ -268,3 +268,15 @@ def test_empty_problem(mx):
     assert c.numel() == 0 and s.numel() == 0
     out = mx.mxattn_forward_bf16(z, z, z)
     assert out.shape == (1, 2, 0, 128)
+
+
+@pytest.mark.parametrize("N", [1, 2, 31, 127, 128, 129, 255, 256, 257])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_tiny_and_ragged_lengths(mx, orc, N, causal):
+    """Every row against the oracle where the tiling has edge cases: one key, a single partial tile,
+    exactly one tile (no second query tile in the CTA), one row past a tile, odd tile counts."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=3, N=N, seed=100 + N)
+    B, H, _, _ = q.shape
+    g = _gpu_mx(mx, q, k, v, causal=causal).reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
+    ref = _oracle(orc, q, k, v, _all_rows(B * H, N), causal=causal)["out"].reshape(B * H, N, 128)
+    _gate(g.reshape(-1, 128), ref.reshape(-1, 128), f"N={N} causal={causal}")

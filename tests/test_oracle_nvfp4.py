@@ -211,3 +211,19 @@ def test_nvfp4_causal_diagonal_is_the_own_16_token_block(orc):
         Vm[b0:i + 1] = Vb[b0:i + 1]
         ref = p @ Vm / p.sum()
         assert np.abs(r["out"][t] - ref).max() <= 1e-12 * np.abs(ref).max(), i
+
+
+@pytest.mark.parametrize("causal,placement", [(False, 1), (True, 1), (False, 0), (True, 0)])
+def test_nvfp4_replay_of_own_phat_is_identical(orc, causal, placement):
+    """Replay mode: feeding the loop its own P^ reproduces its output bit for bit, so a kernel's dumped P^
+    replayed through it isolates accumulation differences from P^ decisions."""
+    (q, k, v), ops = _fwd_inputs(orc, 12, 1, 300)
+    rows = np.array([[0, i] for i in range(0, 300, 3)])
+    own = orc.forward_nvfp4(*ops, rows, vraw_u16=v, causal=causal, placement=placement, want_phat=True)
+    rep = orc.forward_nvfp4(*ops, rows, vraw_u16=v, causal=causal, placement=placement, phat_in=own["phat"])
+    assert np.array_equal(rep["out"], own["out"]) and np.array_equal(rep["ell"], own["ell"])
+    # and a different P^ changes the output (the replay input is used)
+    alt = own["phat"].copy()
+    alt[:, 0] *= 0.5
+    assert not np.array_equal(orc.forward_nvfp4(*ops, rows, vraw_u16=v, causal=causal, placement=placement,
+                                                phat_in=alt)["out"], own["out"])
