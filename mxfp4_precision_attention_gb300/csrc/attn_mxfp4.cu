@@ -63,14 +63,18 @@ constexpr int kNumBars = 40;
 // one 512-byte atom per 128-row tile (4 blocks of 32 per row, both K halves in
 // one 32-bit TMEM word); NVFP4 has two (8 blocks of 16 per row, one word per
 // 64-wide MMA).
-template <bool kNv>
+template <bool kNv, bool kDiag = false>
 struct Lay {
   static constexpr uint32_t kSfTile = kNv ? 2 * kSfAtomBytes : kSfAtomBytes;  // scale bytes per tile
   static constexpr uint32_t kOffQSF = kOffP + 4 * kTileBytes;                  // 2 tiles
   static constexpr uint32_t kOffKSF = kOffQSF + 2 * kSfTile;                   // kKStages tiles
   static constexpr uint32_t kOffVSF = kOffKSF + kKStages * kSfTile;            // kVStages tiles
   static constexpr uint32_t kOffOnesSF = kOffVSF + kVStages * kSfTile;         // constant atom: scale 1
-  static constexpr uint32_t kOffBars = kOffOnesSF + kSfAtomBytes;
+  // causal MXFP4 kernels: the diagonal tile's bf16 V and bf16 P^ for the
+  // tensor-core diagonal product (128-byte swizzle wants 1024-byte alignment)
+  static constexpr uint32_t kOffDiag = (kOffOnesSF + kSfAtomBytes + 1023) / 1024 * 1024;
+  static constexpr uint32_t kDiagBytes = kDiag ? 65536 : 0;
+  static constexpr uint32_t kOffBars = kDiag ? kOffDiag + kDiagBytes : kOffOnesSF + kSfAtomBytes;
   static constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   // TMEM scale columns (S at 0, O_A and O_B at 128 .. 415)
@@ -92,7 +96,10 @@ constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2 groups]: S holds S_g of 
 constexpr int kBarSEmpty = kBarSFull + 2;         // 4 arrivals: the S buffer was read
 constexpr int kBarPFull = kBarSEmpty + 1;         // [2 groups], 4 arrivals: P^ tile + O rescale ready
 constexpr int kBarODone = kBarPFull + 2;          // [2 groups]: P^V^ into O_g complete
-static_assert(kBarODone + 2 <= kNumBars, "barrier space");
+constexpr int kBarDiagV = kBarODone + 2;          // causal: the diagonal tile's bf16 V landed (group A, then B)
+constexpr int kBarDiagP = kBarDiagV + 1;          // [2 groups], 4 arrivals: the group's bf16 P^ rows written
+constexpr int kBarDiagDone = kBarDiagP + 2;       // [2 groups]: the diagonal product into O_g complete
+static_assert(kBarDiagDone + 2 <= kNumBars, "barrier space");
 
 // TMEM columns
 constexpr uint32_t kColS = 0;
@@ -224,9 +231,13 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
 template <bool kCausal, bool kDump, bool kVariant, bool kNv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vb,
+                     const Params p) {
   static_assert(!kNv || kVariant, "NVFP4 runs as a variant kernel");
-  using L = Lay<kNv>;
+  // causal MXFP4: the diagonal block's P^ x bf16 V runs on the tensor cores
+  constexpr bool kDiagMma = kCausal && !kNv;
+  using L = Lay<kNv, kDiagMma>;
+  constexpr uint32_t kOffDiag = L::kOffDiag;
   constexpr uint32_t kOffQSF = L::kOffQSF, kOffKSF = L::kOffKSF, kOffVSF = L::kOffVSF, kOffOnesSF = L::kOffOnesSF;
   constexpr uint32_t kOffBars = L::kOffBars, kOffMisc = L::kOffMisc, kSfTile = L::kSfTile;
   constexpr uint32_t kColSFQ = L::kColSFQ, kColSFK = L::kColSFK, kColSFP = L::kColSFP, kColSFV = L::kColSFV;
@@ -269,6 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone + g), 1);
     }
     mbar_init(bar(kBarSEmpty), 4);
+    if constexpr (kDiagMma) {
+      mbar_init(bar(kBarDiagV), 1);
+      for (int g = 0; g < 2; g++) {
+        mbar_init(bar(kBarDiagP + g), 4);
+        mbar_init(bar(kBarDiagDone + g), 1);
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -299,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      if constexpr (kDiagMma) prefetch_tmap(&tm_vb);
       const int ng = has_b ? 2 : 1;
       mbar_arrive_expect_tx(bar(kBarQFull), ng * (kTileBytes + kSfTile));
       for (int g = 0; g < ng; g++) {
@@ -792,6 +811,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      __uint_as_float(o[4 * i + 2]) * inv_lo, __uint_as_float(o[4 * i + 3]) * inv_lo);
             }
           }
+        } else if (kDiagMma && !(kVariant && p.causal == 2)) {
+          // The diagonal block's product on the tensor cores: this row's P^ on its
+          // own 32-key block (zero beyond the row and outside the block; exact in
+          // bf16, an E2M1 value times a power of two) times the diagonal tile's
+          // bf16 V rows, one kind::f16 128x128x128 product accumulated into O_g
+          // after its last P^V^. Both groups share one 64 KB region, group A (the
+          // earlier diagonal) first; every wait is bounded.
+          const uint32_t vdiag = sb + kOffDiag;          // [channels 0-63 | 64-127][128 keys][128 B]
+          uint8_t* pdiag = smem + kOffDiag + 32768;      // [keys 0-63 | 64-127][128 rows][128 B]
+          const bool leader = quad == 0 && lane == 0;
+          if (g == 1) wait_uniform(kBarDiagDone + 0, 0);  // group A's product has read the region
+          if (leader && !my_abort) {
+            mbar_arrive_expect_tx(bar(kBarDiagV), 32768);
+            tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV), 0, (Tg - 1) * kTile, bh);
+            tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV), 64, (Tg - 1) * kTile, bh);
+          }
+          {
+            uint32_t pw[16];  // this row's P^ on keys 32*quad .. +31 as bf16 pairs
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float a0 = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
+              const float a1 = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8 + 1))) & 0xFu) * dsc;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+              pw[k / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            const int x = r & 7, own_half = quad >> 1, own_c0 = 4 * (quad & 1);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+              uint8_t* prow = pdiag + h * 16384 + r * 128;
+#pragma unroll
+              for (int c = 0; c < 8; c++) {
+                const int oc = c - own_c0;
+                const bool own = h == own_half && oc >= 0 && oc < 4;
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int t = 0; t < 4; t++)
+                  if (own && oc == t) val = make_uint4(pw[4 * t], pw[4 * t + 1], pw[4 * t + 2], pw[4 * t + 3]);
+                *reinterpret_cast<uint4*>(prow + ((c ^ x) << 4)) = val;
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarDiagP + g));
+          if (leader) {
+            bool ok = !my_abort && mbar_wait(bar(kBarDiagP + g), 0, abort_flag) &&
+                      mbar_wait(bar(kBarDiagV), g, abort_flag);
+            if (ok) {
+              tc_fence_after();
+              const uint32_t idd = idesc_bf16(128, 128, true);
+              const uint32_t pa = sb + kOffDiag + 32768;
+              for (int i = 0; i < 8; i++)
+                mma_bf16(tmem + ocol, smem_desc(pa + (i >> 2) * 16384 + (i & 3) * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(vdiag + i * 2048, 16384, 1024, kSwizzle128B), idd, 1u);
+            } else {
+              record_error(p.status, 4, abort_flag);
+            }
+            tc_commit(bar(kBarDiagDone + g));  // arrives once the product (if any) is complete
+          }
+          wait_uniform(kBarDiagDone + g, 0);
+          tc_fence_after();
+          if (!my_abort) {
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+              uint32_t o[32];
+              tmem_ld32(tl + ocol + 32 * c, o);
+              tmem_wait_ld();
+              reg_fence32(o);
+              if (qrow < N) {
+                float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                  dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                       __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              }
+            }
+          }
         } else {
           // The warp's diagonal block is keys 32*quad .. +31 of tile Tg-1 (its own
           // 32 query rows). Its bf16 V rows pass through shared memory one
@@ -954,6 +1050,15 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
     const uint32_t box[3] = {64, kD, 1};
     if (!encode_tensor_map(&tv, 0, 3, const_cast<void*>(a.v_codes), dims, strides, box, 64)) return cudaErrorInvalidValue;
   }
+  // the bf16 V for the causal diagonal tile (the same map shape as the BF16 path)
+  alignas(64) CUtensorMap tvb = tv;
+  if (a.causal && a.v_bf16 != nullptr) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(N) * kD * 2};
+    const uint32_t box[3] = {64, kTile, 1};
+    if (!encode_tensor_map(&tvb, 1, 3, const_cast<void*>(a.v_bf16), dims, strides, box, 128))
+      return cudaErrorInvalidValue;
+  }
   Params p;
   p.q_scales = static_cast<const uint8_t*>(a.q_scales);
   p.k_scales = static_cast<const uint8_t*>(a.k_scales);
@@ -982,11 +1087,16 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   static bool attr_set[64] = {false};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   constexpr uint32_t kSmemMx = Lay<false>::kSmemBytes, kSmemNv = Lay<true>::kSmemBytes;
+  constexpr uint32_t kSmemMxC = Lay<false, true>::kSmemBytes;  // causal: + the diagonal tiles
   if (!attr_set[dev]) {
-    for (auto fn : {mxfp4_fwd_kernel<false, false, false>, mxfp4_fwd_kernel<true, false, false>,
-                    mxfp4_fwd_kernel<false, true, false>, mxfp4_fwd_kernel<true, true, false>,
-                    mxfp4_fwd_kernel<false, false, true>, mxfp4_fwd_kernel<true, false, true>}) {
+    for (auto fn : {mxfp4_fwd_kernel<false, false, false>, mxfp4_fwd_kernel<false, true, false>,
+                    mxfp4_fwd_kernel<false, false, true>}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMx);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto fn : {mxfp4_fwd_kernel<true, false, false>, mxfp4_fwd_kernel<true, true, false>,
+                    mxfp4_fwd_kernel<true, false, true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMxC);
       if (e != cudaSuccess) return e;
     }
     for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<true, false, true, true>,
@@ -1003,21 +1113,21 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
   if (nv) {
     if (a.causal) {
-      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
-      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
+      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
     } else {
-      if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
-      else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, p);
+      if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
+      else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
     }
   } else if (variant) {
-    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
+    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
   } else if (a.causal) {
-    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
+    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
   } else {
-    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
-    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, p);
+    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
+    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
   }
   return cudaGetLastError();
 }
