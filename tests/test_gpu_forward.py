@@ -280,3 +280,34 @@ def test_forward_tiny_and_ragged_lengths(mx, orc, N, causal):
     g = _gpu_mx(mx, q, k, v, causal=causal).reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
     ref = _oracle(orc, q, k, v, _all_rows(B * H, N), causal=causal)["out"].reshape(B * H, N, 128)
     _gate(g.reshape(-1, 128), ref.reshape(-1, 128), f"N={N} causal={causal}")
+
+
+def test_maximum_heads(mx, orc):
+    """B*H = 65535, the largest the ABI accepts (one grid row per head): quantizers and forward against the oracle
+    on sampled rows of the first, last and a middle head."""
+    B, H, N = 5, 13107, 130
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q, k, v = (torch.randn((B, H, N, 128), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    out = _gpu_mx(mx, q, k, v, causal=True).reshape(B * H, N, 128)
+    heads = [0, 32767, B * H - 1]
+    rows = np.array([[h, i] for h in heads for i in (0, 1, 64, 127, 128, 129)], dtype=np.int64)
+    ridx = torch.tensor(rows[:, 0] * N + rows[:, 1], device="cuda")
+    gr = out.reshape(-1, 128).index_select(0, ridx).cpu().numpy().astype(np.float64)
+    ref = _oracle(orc, q, k, v, rows, causal=True, heads=heads)
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    _gate(gr, ref["out"], "B*H = 65535")
+
+
+def test_long_sequence_single_head(mx, orc):
+    """N = 2^20 keys in one head (8192 key tiles per CTA), non-causal, sampled rows against the oracle."""
+    N = 1 << 20
+    g = torch.Generator(device="cuda").manual_seed(4)
+    q, k, v = (torch.randn((1, 1, N, 128), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    out = _gpu_mx(mx, q, k, v).reshape(N, 128)
+    rows = np.array([[0, i] for i in (0, 1, 4095, 524288, N - 2, N - 1)], dtype=np.int64)
+    gr = out.index_select(0, torch.tensor(rows[:, 1], device="cuda")).cpu().numpy().astype(np.float64)
+    ref = _oracle(orc, q, k, v, rows)
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    _gate(gr, ref["out"], "N = 2^20")
