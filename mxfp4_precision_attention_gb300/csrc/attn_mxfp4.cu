@@ -796,21 +796,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_l = 1.0f / l;
         const float inv_lo = kNv ? inv_l * vdq : inv_l;  // O from the tensor cores carries V's encode factor
         float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
-        if constexpr (!kCausal) {
+        // O / l of the warp's 32 rows to global memory in whole 128-byte lines:
+        // each 32-column chunk goes through the warp's own rows of the group's
+        // two P^ buffers (free: every P^V^ of the group has completed), rows
+        // 0-15 in the first and 16-31 in the second, 16-byte units swizzled by
+        // row % 8; then each store instruction writes four rows' 128 bytes.
+        auto store_rows = [&](float inv) {
+          uint8_t* stg0 = smem + kOffP + 2 * g * kTileBytes + quad * 2048;
+          uint8_t* stg1 = stg0 + kTileBytes;
+          const int64_t row0 = qrow - lane;  // global row of the warp's first row
 #pragma unroll 1
           for (int c = 0; c < 4; c++) {
             uint32_t o[32];
             tmem_ld32(tl + ocol + 32 * c, o);
             tmem_wait_ld();
             reg_fence32(o);
-            if (qrow < N) {
-              float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
+            {
+              uint8_t* mine = (lane < 16 ? stg0 : stg1) + (lane & 15) * 128;
 #pragma unroll
               for (int i = 0; i < 8; i++)
-                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_lo, __uint_as_float(o[4 * i + 1]) * inv_lo,
-                                     __uint_as_float(o[4 * i + 2]) * inv_lo, __uint_as_float(o[4 * i + 3]) * inv_lo);
+                *reinterpret_cast<float4*>(mine + ((i ^ (lane & 7)) << 4)) =
+                    make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
             }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; it++) {
+              const int i = 4 * it + (lane >> 3), u = lane & 7;
+              const float4 val = *reinterpret_cast<const float4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
+              if (row0 + i < N)
+                reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 32 * c)[u] = val;
+            }
+            __syncwarp();  // the staging rows are rewritten by the next chunk
           }
+        };
+        if constexpr (!kCausal) {
+          store_rows(inv_lo);
         } else if (kDiagMma && !(kVariant && p.causal == 2)) {
           // The diagonal block's product on the tensor cores: this row's P^ on its
           // own 32-key block (zero beyond the row and outside the block; exact in
@@ -872,22 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wait_uniform(kBarDiagDone + g, 0);
           tc_fence_after();
-          if (!my_abort) {
-#pragma unroll 1
-            for (int c = 0; c < 4; c++) {
-              uint32_t o[32];
-              tmem_ld32(tl + ocol + 32 * c, o);
-              tmem_wait_ld();
-              reg_fence32(o);
-              if (qrow < N) {
-                float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                  dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                       __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
-              }
-            }
-          }
+          if (!my_abort) store_rows(inv_l);
         } else {
           // The warp's diagonal block is keys 32*quad .. +31 of tile Tg-1 (its own
           // 32 query rows). Its bf16 V rows pass through shared memory one
