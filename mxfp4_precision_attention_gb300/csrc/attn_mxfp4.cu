@@ -234,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vb,
                      const Params p) {
   static_assert(!kNv || kVariant, "NVFP4 runs as a variant kernel");
-  // causal MXFP4: the diagonal block's P^ x bf16 V runs on the tensor cores
-  constexpr bool kDiagMma = kCausal && !kNv;
+  // causal: the diagonal block's P^ x bf16 V runs on the tensor cores
+  constexpr bool kDiagMma = kCausal;
   using L = Lay<kNv, kDiagMma>;
   constexpr uint32_t kOffDiag = L::kOffDiag;
   constexpr uint32_t kOffQSF = L::kOffQSF, kOffKSF = L::kOffKSF, kOffVSF = L::kOffVSF, kOffOnesSF = L::kOffOnesSF;
@@ -848,6 +848,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV), 0, (Tg - 1) * kTile, bh);
             tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV), 64, (Tg - 1) * kTile, bh);
           }
+          if constexpr (kNv) {
+            // O_g holds V^'s encoded units (x e_tV): bring this row to real units
+            // first, so the product with the real bf16 V adds in place and the
+            // store divides by l only
+            const float2 d2 = make_float2(vdq, vdq);
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+              uint32_t o[32];
+              tmem_ld32(tl + ocol + 32 * c, o);
+              tmem_wait_ld();
+              reg_fence32(o);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 y = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), d2);
+                o[i] = __float_as_uint(y.x);
+                o[i + 1] = __float_as_uint(y.y);
+              }
+              tmem_st32(tl + ocol + 32 * c, o);
+            }
+            tmem_wait_st();
+          }
           {
             uint32_t pw[16];  // this row's P^ on keys 32*quad .. +31 as bf16 pairs
 #pragma unroll
@@ -874,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           fence_proxy_async_smem();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarDiagP + g));
           if (leader) {
@@ -1094,6 +1116,7 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   constexpr uint32_t kSmemMx = Lay<false>::kSmemBytes, kSmemNv = Lay<true>::kSmemBytes;
   constexpr uint32_t kSmemMxC = Lay<false, true>::kSmemBytes;  // causal: + the diagonal tiles
+  constexpr uint32_t kSmemNvC = Lay<true, true>::kSmemBytes;
   if (!attr_set[dev]) {
     for (auto fn : {mxfp4_fwd_kernel<false, false, false>, mxfp4_fwd_kernel<false, true, false>,
                     mxfp4_fwd_kernel<false, false, true>}) {
@@ -1105,9 +1128,12 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMxC);
       if (e != cudaSuccess) return e;
     }
-    for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<true, false, true, true>,
-                    mxfp4_fwd_kernel<false, true, true, true>, mxfp4_fwd_kernel<true, true, true, true>}) {
+    for (auto fn : {mxfp4_fwd_kernel<false, false, true, true>, mxfp4_fwd_kernel<false, true, true, true>}) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemNv);
+      if (e != cudaSuccess) return e;
+    }
+    for (auto fn : {mxfp4_fwd_kernel<true, false, true, true>, mxfp4_fwd_kernel<true, true, true, true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemNvC);
       if (e != cudaSuccess) return e;
     }
     attr_set[dev] = true;
@@ -1119,8 +1145,8 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
   if (nv) {
     if (a.causal) {
-      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
-      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
+      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, p);
+      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, p);
     } else {
       if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
       else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
