@@ -331,9 +331,8 @@ def mxattn_set_debug_flags(flags: int) -> None:
 
 
 def mxattn_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, stream=None):
-    """The whole hot path on device tensors: rotate+quantize Q and K, quantize V, forward."""
+    """The whole hot path on device tensors: rotate+quantize Q and K and quantize V
+    (one launch), then the forward."""
     B, H, N, _ = _shape(q)
-    qc, qs = mxattn_rotate_quantize_qk(q, stream=stream)
-    kc, ks = mxattn_rotate_quantize_qk(k, stream=stream)
-    vc, vs = mxattn_quantize_v(v, stream=stream)
+    qc, qs, kc, ks, vc, vs = mxattn_quantize_qkv(q, k, v, stream=stream)
     return mxattn_forward(qc, qs, kc, ks, vc, vs, v, B, H, N, causal=causal, stream=stream)

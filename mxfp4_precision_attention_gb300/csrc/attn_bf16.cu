@@ -58,6 +58,7 @@ struct Params {
   int causal;
   uint32_t debug_flags;
   float score_scale_log2;
+  int bh_major;  // grid x walks heads and y walks query tiles (causal), else the reverse
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -98,8 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int bh = blockIdx.y;
-  const int qt = p.causal ? (p.NT - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = static_cast<int>(p.bh_major ? blockIdx.x : blockIdx.y);
+  const int slot = static_cast<int>(p.bh_major ? blockIdx.y : blockIdx.x);
+  const int qt = p.causal ? (p.NT - 1 - slot) : slot;  // causal: heaviest query tiles first
   const int T = p.causal ? qt + 1 : p.NT;
   const int64_t N = p.N;
 
@@ -374,13 +376,20 @@ cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s) {
   p.causal = a.causal;
   p.debug_flags = a.debug_flags;
   p.score_scale_log2 = 1.4426950408889634f / 11.313708498984761f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bf16_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(bf16_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
+  // causal: heads on x so that every head's longest query tile starts first
+  p.bh_major = (a.causal && NT <= 65535) ? 1 : 0;
+  dim3 grid = p.bh_major ? dim3(static_cast<unsigned>(BH), static_cast<unsigned>(NT))
+                         : dim3(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
   bf16_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -133,6 +133,7 @@ struct Params {
   const float* q_amax;     // NVFP4 kernels: the operands' tensor maxima (device)
   const float* k_amax;
   const float* v_amax;
+  int bh_major;  // grid x walks heads and y walks query-tile pairs (causal), else the reverse
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -251,10 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int bh = blockIdx.y;
+  const int bh = static_cast<int>(p.bh_major ? blockIdx.x : blockIdx.y);
+  const int slot = static_cast<int>(p.bh_major ? blockIdx.y : blockIdx.x);
   const int npairs = (p.NT + 1) / 2;
   // causal: heaviest query tiles first
-  const int pair = kCausal ? (npairs - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int pair = kCausal ? (npairs - 1 - slot) : slot;
   const int qtile0 = 2 * pair, qtile1 = 2 * pair + 1;
   const bool has_b = qtile1 < p.NT;
   const int ntiles0 = kCausal ? qtile0 + 1 : p.NT;
@@ -1138,7 +1140,14 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
     }
     attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>((NT + 1) / 2), static_cast<unsigned>(BH));
+  // Blocks start in grid order, x fastest. Non-causal items all cost the same, and
+  // putting the pairs of one head side by side keeps that head's K/V hot in L2.
+  // Causal items cost 2*pair + 2 key tiles: with heads on x every head's longest
+  // pair starts first and the short ones fill the last wave (longest first).
+  const int64_t npairs = (NT + 1) / 2;
+  p.bh_major = (a.causal && npairs <= 65535) ? 1 : 0;
+  dim3 grid = p.bh_major ? dim3(static_cast<unsigned>(BH), static_cast<unsigned>(npairs))
+                         : dim3(static_cast<unsigned>(npairs), static_cast<unsigned>(BH));
   const bool dump = a.phat_codes != nullptr;
   const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ || a.causal == 2;
   if (!nv && variant && dump) return cudaErrorNotSupported;  // the MXFP4 P^ dump covers UOS + PNQ only

@@ -248,6 +248,14 @@ def test_host_entry_point_matches_device_path(mx):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_device_convenience_call_matches_device_path(mx, causal):
+    """mxattn_attention (one quantizer launch, then the forward) gives the
+    output of the separate single-tensor quantizers and the forward, bit for bit."""
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=333)
+    assert torch.equal(mx.mxattn_attention(q, k, v, causal=causal), _gpu_mx(mx, q, k, v, causal=causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_host_entry_point_pipelined_chunks(mx, causal):
     """21 heads run as 16 chunks (one head in the first and in the last) whose
     copies overlap the kernels; two calls in a row (the internal streams and
