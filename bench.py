@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MXFP4 attention fwd TFLOPS and % of GB300 dense FP4 peak (Wan-shaped N=32760)"
 UNIT = "TFLOPS"
 FP4_OVER_BF16_NOMINAL = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rate on GB300
+NOMINAL_FP4_TFLOPS = 13500.0  # nominal dense FP4 tensor rate of one GB300
 
 
 # DRAM bytes of one forward launch from an ncu capture (dram__bytes_read.sum,
@@ -386,6 +387,43 @@ def run_ours(args, w):
                       "frac_of_fp4_peak": nt / fp4_peak, "quantize_ms": nq_ms, "mxfp4_speedup": nf_ms / fwd_ms}
         del qt, kt, vt
 
+    # the dense FP4 MMA rate of this GPU (not part of the step): the tensor-core
+    # probe's back-to-back kind::mxf4 M128 K64 MMAs, N = 256 and the forward's
+    # own N = 128, for about a second each
+    mma_probe = None
+    if not args.no_mma_probe:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mma_probe = {"kernel": "mxf4_mma_rate_kernel (tcgen05 kind::mxf4 M128 Nn K64 back to back, one CTA per SM)",
+                     "nominal_dense_fp4_tflops": NOMINAL_FP4_TFLOPS, "forward_tflops": fwd_tflops}
+        for n in (256, 128):
+            p_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                mx.mxattn_mxf4_mma_rate(2000, n=n, stream=stream)
+                p_ev[0].record(stream)
+                mx.mxattn_mxf4_mma_rate(20000, n=n, stream=stream)
+                p_ev[1].record(stream)
+            torch.cuda.synchronize()
+            mx.mxattn_check(stream)
+            per_iter_ms = p_ev[0].elapsed_time(p_ev[1]) / 20000
+            iters = int(min(1 << 27, max(20000, args.mma_probe_s * 1e3 / per_iter_ms)))
+            probe_clocks = ClockSampler(local)
+            probe_clocks.start()
+            with torch.cuda.stream(stream):
+                p_ev[0].record(stream)
+                pfl = mx.mxattn_mxf4_mma_rate(iters, n=n, stream=stream)
+                p_ev[1].record(stream)
+            torch.cuda.synchronize()
+            pclk = probe_clocks.stop()
+            mx.mxattn_check(stream)
+            pms = p_ev[0].elapsed_time(p_ev[1])
+            pt = pfl / (pms * 1e-3) / 1e12
+            mhz = pclk.get("sm_mhz")
+            mma_probe[f"n{n}"] = {
+                "tflops": pt, "ms": pms, "iters_per_cta": iters, "clocks": pclk,
+                "frac_of_nominal": pt / NOMINAL_FP4_TFLOPS,
+                "flop_per_clock_per_sm": pt * 1e12 / (sms * mhz * 1e6) if mhz else None,
+                "forward_frac": fwd_tflops / pt}
+
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
     if not args.no_e2e:
@@ -436,6 +474,7 @@ def run_ours(args, w):
             "gpu_launches": 2 * args.steps,
             "bf16_path": bf16_path,
             "nvfp4_path": nvfp4_path,
+            "fp4_mma_probe": mma_probe,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -692,6 +731,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison-path timing")
     ap.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4 comparison-path timing")
+    ap.add_argument("--no-mma-probe", action="store_true", help="skip the dense FP4 MMA rate probe")
+    ap.add_argument("--mma-probe-s", type=float, default=1.0, help="seconds of back-to-back MMAs in the probe")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--accuracy", action="store_true",

@@ -270,6 +270,26 @@ MXATTN_API mxattn_status mxattn_attention_noalloc(const void* q, const void* k, 
                                                   int64_t N, int64_t D, int causal, float* out, void* stream);
 MXATTN_API size_t mxattn_attention_noalloc_max_scratch_bytes(void);
 
+/* Tensor-core rate probe (measurement only; not a step of the attention).
+ * Launches one CTA per SM on `stream`; each issues `iters` iterations of two
+ * back-to-back tcgen05.mma kind::mxf4.block_scale.scale_vec::2X, M128 Nn
+ * K64, E2M1 operands from shared memory and UE8M0 scales of 2^0 in TMEM, with
+ * no other work, so that the caller's event timing of the launch gives the
+ * dense FP4 (MXFP4) MMA rate of the device. The rate is the denominator
+ * against which the tensor-core share of the attention forward (the QK^T and
+ * P^V^ products of "MXAttention", Algorithm 2) is read; n = 128 is the
+ * forward's own MMA shape.
+ *   iters      1 .. 2^27 iterations per CTA (else MXATTN_ERR_INVALID_ARG).
+ *   n          128 or 256 (else MXATTN_ERR_INVALID_ARG).
+ *   d_out      optional device float[128*n], written with CTA 0's
+ *              accumulator D[r][j] = 128 * iters * a_r * b_j, where a_r is the
+ *              E2M1 value of code (7r+1) mod 16 and b_j of code (11j+5) mod 16
+ *              (row-major, caller-owned, 4-byte aligned; NULL to skip).
+ *   flops_out  optional host double: the launch's FLOP count,
+ *              SMs * iters * 2 * (2*128*n*64).
+ * A bounded wait that expires sets the status word read by mxattn_check. */
+MXATTN_API mxattn_status mxattn_mxf4_mma_rate(int64_t iters, int n, float* d_out, double* flops_out, void* stream);
+
 /* Synchronize `stream`, then read and clear the device status word that the
  * attention kernels set when a bounded wait expires. Returns MXATTN_OK,
  * MXATTN_ERR_TIMEOUT or MXATTN_ERR_CUDA. */

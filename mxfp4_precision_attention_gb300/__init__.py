@@ -79,12 +79,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_attention_noalloc_max_scratch_bytes.argtypes = []
         lib.mxattn_attention_noalloc_max_scratch_bytes.restype = SZ
         lib.mxattn_check.argtypes = [P]
+        lib.mxattn_mxf4_mma_rate.argtypes = [I64, I, P, ctypes.POINTER(Dbl), P]
         lib.mxattn_set_debug_flags.argtypes = [U32]
         lib.mxattn_set_debug_flags.restype = None
         lib.mxattn_last_error.restype = ctypes.c_char_p
         for name in ("mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward", "mxattn_forward_dump_phat",
                      "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_check", "mxattn_quantize_qk_ex",
-                     "mxattn_quantize_v_ex", "mxattn_forward_ex"):
+                     "mxattn_quantize_v_ex", "mxattn_forward_ex", "mxattn_mxf4_mma_rate"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -324,6 +325,18 @@ def mxattn_attention_noalloc_max_scratch_bytes() -> int:
 def mxattn_check(stream=None) -> None:
     """Synchronize and raise MxattnError if a kernel reported an expired bounded wait."""
     _raise(load().mxattn_check(_stream(stream)))
+
+
+def mxattn_mxf4_mma_rate(iters: int, n: int = 256, out: torch.Tensor | None = None, stream=None) -> float:
+    """Launch the tensor-core rate probe (one CTA per SM, `iters` pairs of
+    M128 Nn K64 kind::mxf4 MMAs each, n = 128 or 256) and return the launch's
+    FLOP count. `out`, a device float32 [128, n], receives CTA 0's accumulator."""
+    if out is not None and (out.dtype != torch.float32 or out.numel() != 128 * n or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous float32 tensor of 128*n elements")
+    flops = ctypes.c_double(0.0)
+    _raise(load().mxattn_mxf4_mma_rate(int(iters), int(n), _ptr(out) if out is not None else None,
+                                       ctypes.byref(flops), _stream(stream)))
+    return flops.value
 
 
 def mxattn_set_debug_flags(flags: int) -> None:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxattn.so")
-SOURCES = ["quantize.cu", "attn_mxfp4.cu", "attn_bf16.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["quantize.cu", "attn_mxfp4.cu", "attn_bf16.cu", "api.cu", "noalloc.cu", "mma_rate.cu"]
 HEADERS = ["sm103_ptx.cuh", "internal.h"]
 
 NVCC_FLAGS = [

@@ -590,6 +590,21 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
   return MXATTN_OK;
 }
 
+mxattn_status mxattn_mxf4_mma_rate(int64_t iters, int n, float* d_out, double* flops_out, void* stream) {
+  t_err[0] = '\0';
+  if (iters < 1 || iters > (int64_t(1) << 27))
+    return fail(MXATTN_ERR_INVALID_ARG, "iters=%lld outside [1, 2^27]", (long long)iters);
+  if (n != 128 && n != 256) return fail(MXATTN_ERR_INVALID_ARG, "n=%d must be 128 or 256", n);
+  if (d_out != nullptr && (reinterpret_cast<uintptr_t>(d_out) & 3u) != 0)
+    return fail(MXATTN_ERR_INVALID_ARG, "d_out is not 4-byte aligned");
+  if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
+  int ctas = 0;
+  cudaError_t e = launch_mxf4_mma_rate(iters, n, d_out, &ctas, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mma rate probe launch");
+  if (flops_out != nullptr) *flops_out = mxf4_mma_rate_flops(iters, n, ctas);
+  return MXATTN_OK;
+}
+
 mxattn_status mxattn_check(void* stream) {
   int st = 0;
   cudaError_t e = read_and_clear_device_status(&st, static_cast<cudaStream_t>(stream));

@@ -82,6 +82,11 @@ struct Bf16FwdArgs {
 };
 cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s);
 
+// Tensor-core rate probe (mma_rate.cu): one CTA per SM, `iters` pairs of
+// M128 Nn K64 kind::mxf4 MMAs each (n = 128 or 256); *ctas_out = the grid size.
+cudaError_t launch_mxf4_mma_rate(int64_t iters, int n, float* d_out, int* ctas_out, cudaStream_t s);
+double mxf4_mma_rate_flops(int64_t iters, int n, int ctas);
+
 // Device status word written by kernels whose bounded waits expired.
 cudaError_t read_and_clear_device_status(int* status, cudaStream_t s);
 int* device_status_ptr();

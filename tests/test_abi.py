@@ -95,6 +95,12 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.mxattn_attention_host(fake, fake, fake, 1, 1, 128, 128, 0, fake, big[0], 16, None) == 1
     assert lib.mxattn_attention_host(fake, fake, fake, 1, 1, 128, 128, 0, fake, ctypes.c_void_p(0x1000010),
                                      1 << 30, None) == 1
+    # tensor-core rate probe: iteration count out of range, misaligned accumulator buffer
+    assert lib.mxattn_mxf4_mma_rate(0, 256, None, None, None) == 1
+    assert lib.mxattn_mxf4_mma_rate((1 << 27) + 1, 256, None, None, None) == 1
+    assert "iters" in _err(lib)
+    assert lib.mxattn_mxf4_mma_rate(10, 192, None, None, None) == 1
+    assert lib.mxattn_mxf4_mma_rate(10, 256, ctypes.c_void_p(0x10002), None, None) == 1
 
 
 def test_empty_problem_is_a_no_op(lib):
