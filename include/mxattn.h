@@ -122,6 +122,17 @@ MXATTN_API mxattn_status mxattn_forward(const void* q_codes, const void* q_scale
                              const void* v_codes, const void* v_scales, const void* v_bf16, int64_t B, int64_t H,
                              int64_t N, int64_t D, int causal, float* out, void* stream);
 
+/* mxattn_forward with the output O = O / l (the finalize step of
+ * "MXAttention" Algorithm 2, Eq. 8) written as bf16 instead of fp32: each
+ * element is the fp32 value mxattn_forward writes, rounded to the nearest
+ * bf16 (ties to even).
+ *   out : bf16 [B, H, N, 128] (device, written, 16-byte aligned)
+ * Same other arguments and errors as mxattn_forward (causal 0 or 1). */
+MXATTN_API mxattn_status mxattn_forward_out_bf16(const void* q_codes, const void* q_scales, const void* k_codes,
+                                                 const void* k_scales, const void* v_codes, const void* v_scales,
+                                                 const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D,
+                                                 int causal, void* out, void* stream);
+
 /* Diagnostic variant of mxattn_forward that also writes every P^ tile:
  *   phat_codes  [B*H][N][ceil(N/128)*64]: E2M1 codes of tile j at bytes
  *               64j..64j+63 (key 2i of the tile in the low nibble of byte i);

@@ -68,6 +68,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                        P, P]
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
+        lib.mxattn_forward_out_bf16.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
         Dbl = ctypes.c_double
         lib.mxattn_quantize_qk_ex.argtypes = [P, I64, I64, I64, I64, I, Dbl, I, P, P, P]
@@ -85,7 +86,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_last_error.restype = ctypes.c_char_p
         for name in ("mxattn_rotate_quantize_qk", "mxattn_quantize_v", "mxattn_forward", "mxattn_forward_dump_phat",
                      "mxattn_forward_bf16", "mxattn_attention_host", "mxattn_check", "mxattn_quantize_qk_ex",
-                     "mxattn_quantize_v_ex", "mxattn_forward_ex", "mxattn_mxf4_mma_rate"):
+                     "mxattn_quantize_v_ex", "mxattn_forward_ex", "mxattn_mxf4_mma_rate",
+                     "mxattn_forward_out_bf16"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -213,12 +215,19 @@ def mxattn_nvfp4_forward_dump_phat(q, k, v, v_bf16, B: int, H: int, N: int, caus
 
 
 def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
-                   causal: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """MXFP4 attention forward with PNQ on quantized operands. Returns fp32 [B, H, N, 128]."""
+                   causal: bool = False, out: torch.Tensor | None = None, stream=None,
+                   out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """MXFP4 attention forward with PNQ on quantized operands. Returns [B, H, N, 128]
+    in `out_dtype`: float32, or bfloat16 (the float32 result rounded to nearest even)."""
     dev = q_codes.device
-    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
-    _raise(load().mxattn_forward(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
-                                 _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), _ptr(out), _stream(stream)))
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    out = torch.empty((B, H, N, D), dtype=out_dtype, device=dev) if out is None else out
+    if out.dtype != out_dtype:
+        raise ValueError("out does not have out_dtype")
+    fn = load().mxattn_forward if out_dtype == torch.float32 else load().mxattn_forward_out_bf16
+    _raise(fn(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+              _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), _ptr(out), _stream(stream)))
     return out
 
 

@@ -111,9 +111,9 @@ mxattn_status check_quantizer_runtime() {
 
 mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const void* ks, const void* vc,
                            const void* vs, const void* vb, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
-                           float* out, uint8_t* pc, uint8_t* ps, void* stream, int p_rule = kRuleUOS,
+                           void* out, uint8_t* pc, uint8_t* ps, void* stream, int p_rule = kRuleUOS,
                            int placement = kPlacePNQ, double p_qmax = 7.25, const float* q_amax = nullptr,
-                           const float* k_amax = nullptr, const float* v_amax = nullptr) {
+                           const float* k_amax = nullptr, const float* v_amax = nullptr, bool out_bf16 = false) {
   bool empty = false;
   MX_TRY(check_shape(B, H, N, D, &empty));
   if (empty) return MXATTN_OK;
@@ -136,7 +136,7 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   }
   const bool nv = q_amax != nullptr;
   const size_t sfb = (nv ? 2 : 1) * sf_bytes(B, H, N);
-  const Range ro = rng(out, f32_bytes(B, H, N));
+  const Range ro = rng(out, out_bf16 ? bf16_bytes(B, H, N) : f32_bytes(B, H, N));
   const Range ins[] = {rng(qc, qk_codes(B, H, N)), rng(qs, sfb), rng(kc, qk_codes(B, H, N)),
                        rng(ks, sfb),  rng(vc, v_codes(B, H, N)), rng(vs, sfb)};
   for (const Range& r : ins)
@@ -162,7 +162,8 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
   a.BH = B * H;
   a.N = N;
   a.causal = causal;
-  a.out = out;
+  a.out = out_bf16 ? nullptr : static_cast<float*>(out);
+  a.out_bf16 = out_bf16 ? out : nullptr;
   a.phat_codes = pc;
   a.phat_scales = ps;
   a.debug_flags = g_debug_flags;
@@ -410,6 +411,16 @@ mxattn_status mxattn_forward(const void* q_codes, const void* q_scales, const vo
   if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
                       nullptr, nullptr, stream);
+}
+
+mxattn_status mxattn_forward_out_bf16(const void* q_codes, const void* q_scales, const void* k_codes,
+                                      const void* k_scales, const void* v_codes, const void* v_scales,
+                                      const void* v_bf16, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                                      void* out, void* stream) {
+  t_err[0] = '\0';
+  if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  return forward_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, D, causal, out,
+                      nullptr, nullptr, stream, kRuleUOS, kPlacePNQ, 7.25, nullptr, nullptr, nullptr, true);
 }
 
 mxattn_status mxattn_forward_dump_phat(const void* q_codes, const void* q_scales, const void* k_codes,

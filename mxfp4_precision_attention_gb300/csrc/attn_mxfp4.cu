@@ -117,6 +117,7 @@ struct Params {
   const uint8_t* v_scales;
   const __nv_bfloat16* v_bf16;
   float* out;
+  __nv_bfloat16* out_bf16;  // non-null: O / l is written here as bf16 instead of to `out`
   uint8_t* phat_codes;
   uint8_t* phat_scales;
   int* status;
@@ -135,6 +136,13 @@ struct Params {
   const float* v_amax;
   int bh_major;  // grid x walks heads and y walks query-tile pairs (causal), else the reverse
 };
+
+// two fp32 values -> bf16x2 (round to nearest even), `lo` in the low half
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -229,7 +237,7 @@ __device__ __forceinline__ void record_error(int* status, int code, volatile int
 // floor of Eq. 11, TFS of Eq. 14, or the ceil rule with a swept Q_max of
 // section 5.5.1) and l may come from the unquantized P~
 // (direct placement, Eqs. 16-17) instead of P^ (PNQ, Eq. 47).
-template <bool kCausal, bool kDump, bool kVariant, bool kNv = false>
+template <bool kCausal, bool kDump, bool kVariant, bool kNv = false, bool kBf16Out = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vb,
@@ -622,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
       } else {
         float bm[4];
-  #pragma unroll
+#pragma unroll
         for (int b = 0; b < 4; b++) bm[b] = max32(v + 32 * b);
         m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
         const float mc = m_new * C;
@@ -674,20 +682,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
         if (masked) {
           // all-zero (fully masked) blocks take sigma = 1
-  #pragma unroll
+#pragma unroll
           for (int b = 0; b < 4; b++)
             if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
         }
-  #pragma unroll
+#pragma unroll
         for (int b = 0; b < 4; b++) {
           const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
           const float2 noff2 = make_float2(noff, noff);
           uint32_t w[4];
           float2 ysum = make_float2(0.0f, 0.0f);
-  #pragma unroll
+#pragma unroll
           for (int gq = 0; gq < 4; gq++) {
             float y[8];
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 8; i += 2) {
               const float2 x = __ffma2_rn(make_float2(v[32 * b + 8 * gq + i], v[32 * b + 8 * gq + i + 1]), c2, noff2);
               y[i] = ex2_approx(x.x);
@@ -706,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (diag_tile && b == quad) {
             // the query's own 32-key block: keep its codes for the bf16-V product,
             // drop it from the tensor-core operand
-  #pragma unroll
+#pragma unroll
             for (int gq = 0; gq < 4; gq++) {
               diag_words[gq] = w[gq];
               w[gq] = 0u;
@@ -807,29 +815,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* stg0 = smem + kOffP + 2 * g * kTileBytes + quad * 2048;
           uint8_t* stg1 = stg0 + kTileBytes;
           const int64_t row0 = qrow - lane;  // global row of the warp's first row
+          if constexpr (kBf16Out) {
+            // bf16 output: a pass covers 64 columns, again 128 bytes of a row
 #pragma unroll 1
-          for (int c = 0; c < 4; c++) {
-            uint32_t o[32];
-            tmem_ld32(tl + ocol + 32 * c, o);
-            tmem_wait_ld();
-            reg_fence32(o);
-            {
-              uint8_t* mine = (lane < 16 ? stg0 : stg1) + (lane & 15) * 128;
+            for (int c = 0; c < 2; c++) {
+              uint32_t o[32], o2[32];
+              tmem_ld32(tl + ocol + 64 * c, o);
+              tmem_ld32(tl + ocol + 64 * c + 32, o2);
+              tmem_wait_ld();
+              reg_fence32(o);
+              reg_fence32(o2);
+              {
+                uint8_t* mine = (lane < 16 ? stg0 : stg1) + (lane & 15) * 128;
+                auto pk = [&](const uint32_t* x) {
+                  return make_uint4(bf16x2_rn(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                    bf16x2_rn(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                    bf16x2_rn(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                    bf16x2_rn(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+                };
 #pragma unroll
-              for (int i = 0; i < 8; i++)
-                *reinterpret_cast<float4*>(mine + ((i ^ (lane & 7)) << 4)) =
-                    make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-            }
-            __syncwarp();
+                for (int i = 0; i < 4; i++) *reinterpret_cast<uint4*>(mine + ((i ^ (lane & 7)) << 4)) = pk(o + 8 * i);
 #pragma unroll
-            for (int it = 0; it < 8; it++) {
-              const int i = 4 * it + (lane >> 3), u = lane & 7;
-              const float4 val = *reinterpret_cast<const float4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
-              if (row0 + i < N)
-                reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 32 * c)[u] = val;
+                for (int i = 4; i < 8; i++)
+                  *reinterpret_cast<uint4*>(mine + ((i ^ (lane & 7)) << 4)) = pk(o2 + 8 * (i - 4));
+              }
+              __syncwarp();
+#pragma unroll
+              for (int it = 0; it < 8; it++) {
+                const int i = 4 * it + (lane >> 3), u = lane & 7;
+                const uint4 val = *reinterpret_cast<const uint4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
+                if (row0 + i < N)
+                  reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 64 * c)[u] = val;
+              }
+              __syncwarp();
             }
-            __syncwarp();  // the staging rows are rewritten by the next chunk
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+              uint32_t o[32];
+              tmem_ld32(tl + ocol + 32 * c, o);
+              tmem_wait_ld();
+              reg_fence32(o);
+              {
+                uint8_t* mine = (lane < 16 ? stg0 : stg1) + (lane & 15) * 128;
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                  *reinterpret_cast<float4*>(mine + ((i ^ (lane & 7)) << 4)) =
+                      make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                  __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int it = 0; it < 8; it++) {
+                const int i = 4 * it + (lane >> 3), u = lane & 7;
+                const float4 val = *reinterpret_cast<const float4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
+                if (row0 + i < N)
+                  reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 32 * c)[u] = val;
+              }
+              __syncwarp();  // the staging rows are rewritten by the next chunk
+            }
           }
         };
         if constexpr (!kCausal) {
@@ -1095,6 +1139,7 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   p.v_scales = static_cast<const uint8_t*>(a.v_scales);
   p.v_bf16 = static_cast<const __nv_bfloat16*>(a.v_bf16);
   p.out = a.out;
+  p.out_bf16 = static_cast<__nv_bfloat16*>(a.out_bf16);
   p.phat_codes = a.phat_codes;
   p.phat_scales = a.phat_scales;
   p.status = device_status_ptr();
@@ -1138,6 +1183,12 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemNvC);
       if (e != cudaSuccess) return e;
     }
+    e = cudaFuncSetAttribute(mxfp4_fwd_kernel<false, false, false, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMx);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mxfp4_fwd_kernel<true, false, false, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMxC);
+    if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   // Blocks start in grid order, x fastest. Non-causal items all cost the same, and
@@ -1152,6 +1203,12 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   const bool variant = a.p_rule != kRuleUOS || a.placement != kPlacePNQ || a.causal == 2;
   if (!nv && variant && dump) return cudaErrorNotSupported;  // the MXFP4 P^ dump covers UOS + PNQ only
   if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
+  if (a.out_bf16 != nullptr) {  // bf16 output: the plain MXFP4 kernels only (UOS, PNQ, no dump)
+    if (nv || variant || dump) return cudaErrorNotSupported;
+    if (a.causal) mxfp4_fwd_kernel<true, false, false, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
+    else mxfp4_fwd_kernel<false, false, false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
+    return cudaGetLastError();
+  }
   if (nv) {
     if (a.causal) {
       if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, p);

@@ -57,6 +57,7 @@ struct Mxfp4FwdArgs {
   int64_t BH, N;
   int causal;  // 0, 1, or 2: diagonal V block re-quantized over the prefix (variant kernel)
   float* out;
+  void* out_bf16;        // non-null (and out null): O / l written as bf16 [BH][N][128] here
   uint8_t* phat_codes;   // optional diagnostic dump, [BH][N][ceil(N/128)*64]
   uint8_t* phat_scales;  // optional diagnostic dump, [BH][N][ceil(N/128)*4]
   uint32_t debug_flags;

@@ -89,6 +89,8 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.mxattn_forward(*big[:6], None, 1, 1, 128, 128, 1, big[6], None) == 1
     assert "v_bf16" in _err(lib)
     assert lib.mxattn_forward(*big[:6], None, 1, 1, 128, 128, 2, big[6], None) == 1
+    assert lib.mxattn_forward_out_bf16(*big[:6], big[7], 1, 1, 128, 128, 2, big[6], None) == 1
+    assert lib.mxattn_forward_out_bf16(*big[:6], None, 1, 1, 128, 128, 1, big[6], None) == 1
     # dump needs both buffers
     assert lib.mxattn_forward_dump_phat(*big[:6], None, 1, 1, 128, 128, 0, big[6], big[7], None, None) == 1
     # host entry: workspace too small / misaligned

@@ -319,3 +319,28 @@ def test_long_sequence_single_head(mx, orc):
     del q, k, v, out
     torch.cuda.empty_cache()
     _gate(gr, ref["out"], "N = 2^20")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 333, 1000])
+def test_bf16_output_is_the_rounded_fp32_output(mx, N, causal):
+    """mxattn_forward_out_bf16 writes exactly the fp32 output rounded to the
+    nearest bf16 (ties to even), rows < N only."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=3, N=N, seed=200 + N)
+    qc, qs, kc, ks, vc, vs = mx.mxattn_quantize_qkv(q, k, v)
+    o32 = mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 3, N, causal=causal)
+    o16 = mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 3, N, causal=causal, out_dtype=torch.bfloat16)
+    mx.mxattn_check()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_bf16_output_full_length(mx):
+    w = W.WORKLOADS["wan_32760"]
+    q, k, v = W.generate(w, device="cuda", H=4)
+    qc, qs, kc, ks, vc, vs = mx.mxattn_quantize_qkv(q, k, v)
+    o32 = mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 4, w.N)
+    o16 = torch.full(o32.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 4, w.N, out=o16, out_dtype=torch.bfloat16)
+    mx.mxattn_check()
+    assert torch.equal(o16, o32.to(torch.bfloat16))
