@@ -805,7 +805,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (direct) l = l_direct;
         const float inv_l = 1.0f / l;
         const float inv_lo = kNv ? inv_l * vdq : inv_l;  // O from the tensor cores carries V's encode factor
-        float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
         // O / l of the warp's 32 rows to global memory in whole 128-byte lines:
         // each 32-column chunk goes through the warp's own rows of the group's
         // two P^ buffers (free: every P^V^ of the group has completed), rows
@@ -971,6 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // staging space is this group's two P^ buffers, idle since the o_done
           // wait above (every P^V^ that read them has completed): 4 KB per warp,
           // two chunk slots.
+          float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
           uint8_t* stage = smem + kOffP + 2 * g * kTileBytes + quad * 4096;
           const int64_t mykey = static_cast<int64_t>(Tg - 1) * kTile + 32 * quad + lane;
           const bool key_ok = mykey < N;
