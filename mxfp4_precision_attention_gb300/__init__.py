@@ -116,6 +116,48 @@ def _shape(x: torch.Tensor):
     return x.shape
 
 
+def _buf(t, nbytes: int, name: str, device=None, dtype=None) -> None:
+    """A caller-supplied device buffer: a contiguous CUDA tensor on `device`, of
+    `dtype` if given, holding at least `nbytes` bytes. Checked before any launch,
+    so a wrong buffer raises here instead of reaching a kernel."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, not {t.dtype}")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, {nbytes} needed")
+
+
+def _elems(B: int, H: int, N: int) -> int:
+    return max(B, 0) * max(H, 0) * max(N, 0) * D
+
+
+def _check_mx_operands(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, causal,
+                       scales_bytes=None):
+    """The forward's quantized operands (and the bf16 V if given or needed) against B, H, N."""
+    _buf(q_codes, 0, "q_codes")
+    dev = q_codes.device
+    nc, ns = qk_layout_sizes(B, H, N)
+    vc, vs = v_layout_sizes(B, H, N)
+    if scales_bytes is not None:
+        ns = vs = scales_bytes
+    for t, n, name in ((q_codes, nc, "q_codes"), (q_scales, ns, "q_scales"), (k_codes, nc, "k_codes"),
+                       (k_scales, ns, "k_scales"), (v_codes, vc, "v_codes"), (v_scales, vs, "v_scales")):
+        _buf(t, n, name, dev)
+    if causal or v_bf16 is not None:
+        _buf(v_bf16, 2 * _elems(B, H, N), "v_bf16", dev, torch.bfloat16)
+    return dev
+
+
+def _out(out, B, H, N, dtype, dev):
+    if out is None:
+        return torch.empty((max(B, 0), max(H, 0), max(N, 0), D), dtype=dtype, device=dev)
+    _buf(out, _elems(B, H, N) * torch.empty(0, dtype=dtype).element_size(), "out", dev, dtype)
+    return out
+
+
 def qk_layout_sizes(B: int, H: int, N: int) -> tuple[int, int]:
     lib = load()
     return int(lib.mxattn_qk_codes_bytes(B, H, N)), int(lib.mxattn_qk_scales_bytes(B, H, N))
@@ -133,6 +175,8 @@ def mxattn_rotate_quantize_qk(x: torch.Tensor, codes: torch.Tensor | None = None
     nc, ns = qk_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=x.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=x.device) if scales is None else scales
+    _buf(codes, nc, "codes", x.device)
+    _buf(scales, ns, "scales", x.device)
     _raise(load().mxattn_rotate_quantize_qk(_ptr(x), B, H, N, Dx, _ptr(codes), _ptr(scales), _stream(stream)))
     return codes, scales
 
@@ -144,6 +188,8 @@ def mxattn_quantize_v(v: torch.Tensor, codes: torch.Tensor | None = None, scales
     nc, ns = v_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=v.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
+    _buf(codes, nc, "codes", v.device)
+    _buf(scales, ns, "scales", v.device)
     _raise(load().mxattn_quantize_v(_ptr(v), B, H, N, Dx, _ptr(codes), _ptr(scales), _stream(stream)))
     return codes, scales
 
@@ -159,6 +205,13 @@ def mxattn_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out=N
         nc, ns = qk_layout_sizes(B, H, N)
         vc, vs = v_layout_sizes(B, H, N)
         out = tuple(torch.empty(n, dtype=torch.uint8, device=q.device) for n in (nc, ns, nc, ns, vc, vs))
+    if len(out) != 6:
+        raise ValueError("out must hold six buffers")
+    nc, ns = qk_layout_sizes(B, H, N)
+    vc, vs = v_layout_sizes(B, H, N)
+    for t, n, name in zip(out, (nc, ns, nc, ns, vc, vs), ("q_codes", "q_scales", "k_codes", "k_scales", "v_codes",
+                                                          "v_scales")):
+        _buf(t, n, name, q.device)
     _raise(load().mxattn_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, *(_ptr(t) for t in out),
                                       _stream(stream)))
     return tuple(out)
@@ -190,8 +243,11 @@ def mxattn_nvfp4_forward(q, k, v, v_bf16, B: int, H: int, N: int, causal: bool =
                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """NVFP4 forward; q, k, v are the (codes, scales, amax) triples of the NVFP4 quantizers.
     placement 1 (direct, the baseline) or 0 (PNQ). Returns fp32 [B, H, N, 128]."""
-    dev = q[0].device
-    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
+    sb = int(load().mxattn_nvfp4_scales_bytes(B, H, N))
+    dev = _check_mx_operands(q[0], q[1], k[0], k[1], v[0], v[1], v_bf16, B, H, N, causal, scales_bytes=sb)
+    for t, name in ((q[2], "q amax"), (k[2], "k amax"), (v[2], "v amax")):
+        _buf(t, 4, name, dev, torch.float32)
+    out = _out(out, B, H, N, torch.float32, dev)
     _raise(load().mxattn_nvfp4_forward(_ptr(q[0]), _ptr(q[1]), _ptr(q[2]), _ptr(k[0]), _ptr(k[1]), _ptr(k[2]),
                                        _ptr(v[0]), _ptr(v[1]), _ptr(v[2]), _ptr(v_bf16), B, H, N, D, int(causal),
                                        int(placement), _ptr(out), _stream(stream)))
@@ -202,7 +258,10 @@ def mxattn_nvfp4_forward_dump_phat(q, k, v, v_bf16, B: int, H: int, N: int, caus
                                    placement: int = 1, stream=None):
     """mxattn_nvfp4_forward plus every P^ tile: returns (out, phat_codes [B*H, N, NT*64],
     phat_scales [B*H, N, NT*8])."""
-    dev = q[0].device
+    sb = int(load().mxattn_nvfp4_scales_bytes(B, H, N))
+    dev = _check_mx_operands(q[0], q[1], k[0], k[1], v[0], v[1], v_bf16, B, H, N, causal, scales_bytes=sb)
+    for t, name in ((q[2], "q amax"), (k[2], "k amax"), (v[2], "v amax")):
+        _buf(t, 4, name, dev, torch.float32)
     nt = (N + 127) // 128
     out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
     pc = torch.zeros((B * H, N, nt * 64), dtype=torch.uint8, device=dev)
@@ -219,12 +278,10 @@ def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf
                    out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
     """MXFP4 attention forward with PNQ on quantized operands. Returns [B, H, N, 128]
     in `out_dtype`: float32, or bfloat16 (the float32 result rounded to nearest even)."""
-    dev = q_codes.device
     if out_dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
-    out = torch.empty((B, H, N, D), dtype=out_dtype, device=dev) if out is None else out
-    if out.dtype != out_dtype:
-        raise ValueError("out does not have out_dtype")
+    dev = _check_mx_operands(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, causal)
+    out = _out(out, B, H, N, out_dtype, dev)
     fn = load().mxattn_forward if out_dtype == torch.float32 else load().mxattn_forward_out_bf16
     _raise(fn(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
               _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), _ptr(out), _stream(stream)))
@@ -234,7 +291,7 @@ def mxattn_forward(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf
 def mxattn_forward_dump_phat(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B: int, H: int, N: int,
                              causal: bool = False, stream=None):
     """Diagnostic forward that also returns every P^ tile (codes [B*H, N, NT*64], scales [B*H, N, NT*4])."""
-    dev = q_codes.device
+    dev = _check_mx_operands(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, causal)
     NT = (N + 127) // 128
     out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
     pc = torch.zeros((B * H, N, NT * 64), dtype=torch.uint8, device=dev)
@@ -258,6 +315,8 @@ def mxattn_quantize_qk_ex(x: torch.Tensor, rule: int = RULE_UOS, rotate: bool = 
     nc, ns = qk_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=x.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=x.device) if scales is None else scales
+    _buf(codes, nc, "codes", x.device)
+    _buf(scales, ns, "scales", x.device)
     _raise(load().mxattn_quantize_qk_ex(_ptr(x), B, H, N, Dx, int(rule), float(qmax), int(bool(rotate)),
                                         _ptr(codes), _ptr(scales), _stream(stream)))
     return codes, scales
@@ -270,6 +329,8 @@ def mxattn_quantize_v_ex(v: torch.Tensor, rule: int = RULE_UOS, qmax: float = 7.
     nc, ns = v_layout_sizes(B, H, N)
     codes = torch.empty(nc, dtype=torch.uint8, device=v.device) if codes is None else codes
     scales = torch.empty(ns, dtype=torch.uint8, device=v.device) if scales is None else scales
+    _buf(codes, nc, "codes", v.device)
+    _buf(scales, ns, "scales", v.device)
     _raise(load().mxattn_quantize_v_ex(_ptr(v), B, H, N, Dx, int(rule), float(qmax), _ptr(codes), _ptr(scales),
                                        _stream(stream)))
     return codes, scales
@@ -279,8 +340,8 @@ def mxattn_forward_ex(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v
                       causal: bool = False, p_rule: int = RULE_UOS, placement: int = PLACE_PNQ,
                       p_qmax: float = 7.25, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Forward with the P~ scale rule and the l placement as switches. Returns fp32 [B, H, N, 128]."""
-    dev = q_codes.device
-    out = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if out is None else out
+    dev = _check_mx_operands(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v_bf16, B, H, N, causal)
+    out = _out(out, B, H, N, torch.float32, dev)
     _raise(load().mxattn_forward_ex(_ptr(q_codes), _ptr(q_scales), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
                                     _ptr(v_scales), _ptr(v_bf16), B, H, N, D, int(causal), int(p_rule),
                                     float(p_qmax), int(placement), _ptr(out), _stream(stream)))
@@ -291,9 +352,9 @@ def mxattn_forward_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causa
                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """BF16 tcgen05 attention forward (comparison path). Returns fp32 [B, H, N, 128]."""
     B, H, N, Dx = _shape(q)
-    _shape(k)
-    _shape(v)
-    out = torch.empty((B, H, N, D), dtype=torch.float32, device=q.device) if out is None else out
+    if _shape(k) != (B, H, N, Dx) or _shape(v) != (B, H, N, Dx):
+        raise ValueError("q, k and v must have the same shape")
+    out = _out(out, B, H, N, torch.float32, q.device)
     _raise(load().mxattn_forward_bf16(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
                                       _stream(stream)))
     return out
@@ -306,10 +367,14 @@ def mxattn_workspace_bytes(B: int, H: int, N: int) -> int:
 def mxattn_attention_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor, causal: bool,
                           out_host: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
     """Whole forward from host (preferably pinned) bf16 tensors into a host fp32 tensor."""
+    if q_host.dim() != 4:
+        raise ValueError("expected [B, H, N, D] host tensors")
     B, H, N, Dx = q_host.shape
-    for t in (q_host, k_host, v_host, out_host):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("host tensors must be contiguous CPU tensors")
+    for t, dt, name in ((q_host, torch.bfloat16, "q_host"), (k_host, torch.bfloat16, "k_host"),
+                        (v_host, torch.bfloat16, "v_host"), (out_host, torch.float32, "out_host")):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != dt or tuple(t.shape) != (B, H, N, Dx):
+            raise ValueError(f"{name} must be a contiguous CPU {dt} tensor of shape {(B, H, N, Dx)}")
+    _buf(workspace, 0, "workspace")
     _raise(load().mxattn_attention_host(_ptr(q_host), _ptr(k_host), _ptr(v_host), B, H, N, Dx, int(causal),
                                         _ptr(out_host), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
@@ -320,8 +385,9 @@ def mxattn_attention_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
                              stream=None) -> torch.Tensor:
     """Whole forward using the library's fixed device scratch (no allocation by the library or here)."""
     B, H, N, Dx = _shape(q)
-    _shape(k)
-    _shape(v)
+    if _shape(k) != (B, H, N, Dx) or _shape(v) != (B, H, N, Dx):
+        raise ValueError("q, k and v must have the same shape")
+    _buf(out, 4 * _elems(B, H, N), "out", q.device, torch.float32)
     _raise(load().mxattn_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
                                            _stream(stream)))
     return out
@@ -340,8 +406,8 @@ def mxattn_mxf4_mma_rate(iters: int, n: int = 256, out: torch.Tensor | None = No
     """Launch the tensor-core rate probe (one CTA per SM, `iters` pairs of
     M128 Nn K64 kind::mxf4 MMAs each, n = 128 or 256) and return the launch's
     FLOP count. `out`, a device float32 [128, n], receives CTA 0's accumulator."""
-    if out is not None and (out.dtype != torch.float32 or out.numel() != 128 * n or not out.is_contiguous()):
-        raise ValueError("out must be a contiguous float32 tensor of 128*n elements")
+    if out is not None:
+        _buf(out, 4 * 128 * n, "out", dtype=torch.float32)
     flops = ctypes.c_double(0.0)
     _raise(load().mxattn_mxf4_mma_rate(int(iters), int(n), _ptr(out) if out is not None else None,
                                        ctypes.byref(flops), _stream(stream)))

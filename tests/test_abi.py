@@ -136,3 +136,23 @@ def test_variant_switches_rejected_on_host(lib):
     assert lib.mxattn_forward_ex(*big[:6], big[7], 1, 1, 128, 128, 3, 0, 7.25, 0, big[6], None) == 1
     # empty problems stay no-ops through the variant calls too
     assert lib.mxattn_quantize_qk_ex(None, 1, 1, 0, 128, 1, 7.25, 0, None, None, None) == 0
+
+
+def test_binding_rejects_wrong_buffers_before_any_launch():
+    """The Python binding checks caller-supplied buffers (device, dtype, size)
+    before calling into the library; CPU tensors where device buffers belong
+    are refused here, on a machine without a GPU."""
+    import torch
+
+    import mxfp4_precision_attention_gb300 as mx
+
+    u8 = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        mx.mxattn_forward(u8, u8, u8, u8, u8, u8, None, 1, 1, 128)
+    with pytest.raises(ValueError, match="CUDA"):
+        mx.mxattn_mxf4_mma_rate(10, out=torch.zeros(128 * 256))
+    q = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="out_host"):
+        mx.mxattn_attention_host(q, q, q, False, torch.zeros((1, 1, 128, 128), dtype=torch.float16), u8)
+    with pytest.raises(ValueError, match="k_host"):
+        mx.mxattn_attention_host(q, q.float(), q, False, torch.zeros((1, 1, 128, 128)), u8)

@@ -344,3 +344,23 @@ def test_bf16_output_full_length(mx):
     mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 4, w.N, out=o16, out_dtype=torch.bfloat16)
     mx.mxattn_check()
     assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_binding_rejects_short_device_buffers(mx):
+    """Buffers smaller than the layouts of B, H, N raise before any launch."""
+    q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda", N=300)
+    qc, qs, kc, ks, vc, vs = mx.mxattn_quantize_qkv(q, k, v)
+    with pytest.raises(ValueError, match="k_codes"):
+        mx.mxattn_forward(qc, qs, kc[:-1], ks, vc, vs, v, 1, 2, 300)
+    with pytest.raises(ValueError, match="v_bf16"):
+        mx.mxattn_forward(qc, qs, kc, ks, vc, vs, None, 1, 2, 300, causal=True)
+    with pytest.raises(ValueError, match="out"):
+        mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 2, 300, out=torch.empty((1, 2, 299, 128), device="cuda"))
+    with pytest.raises(ValueError, match="dtype"):
+        mx.mxattn_forward(qc, qs, kc, ks, vc, vs, v, 1, 2, 300, out=torch.empty((1, 2, 300, 128), device="cuda"),
+                          out_dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="scales"):
+        mx.mxattn_rotate_quantize_qk(q, scales=qs[:10])
+    with pytest.raises(ValueError, match="v_codes"):
+        mx.mxattn_quantize_qkv(q, k, v, out=(qc, qs, kc, ks, vc[:5], vs))
+    mx.mxattn_check()
