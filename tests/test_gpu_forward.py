@@ -364,3 +364,32 @@ def test_binding_rejects_short_device_buffers(mx):
     with pytest.raises(ValueError, match="v_codes"):
         mx.mxattn_quantize_qkv(q, k, v, out=(qc, qs, kc, ks, vc[:5], vs))
     mx.mxattn_check()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cuda_graph_capture_and_replay(mx, causal):
+    """The two-launch step (one quantizer launch, the forward) captures into a
+    CUDA graph; replays give the eager output bit for bit, and recompute after
+    the inputs are overwritten in place."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=3, N=1000, seed=41)
+    ref = mx.mxattn_attention(q, k, v, causal=causal)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        mx.mxattn_attention(q, k, v, causal=causal, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = mx.mxattn_attention(q, k, v, causal=causal)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    q2, k2, v2 = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=3, N=1000, seed=42)
+    q.copy_(q2)
+    k.copy_(k2)
+    v.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, mx.mxattn_attention(q2, k2, v2, causal=causal))
+    mx.mxattn_check()
