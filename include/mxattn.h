@@ -148,9 +148,15 @@ MXATTN_API mxattn_status mxattn_forward_dump_phat(const void* q_codes, const voi
 /* BF16 comparison path (no rotation, no quantization): the same online
  * softmax recurrence (Eqs. 2-8) with bf16 Q, K, V and P on tcgen05 kind::f16
  * tensor cores and fp32 accumulation; l sums the bf16-rounded P.
- *   q, k, v : bf16 [B, H, N, 128] (device); out : fp32 [B, H, N, 128] (device) */
-MXATTN_API mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
-                                  int64_t D, int causal, float* out, void* stream);
+ *   q       : bf16 [B, H, Nq, 128] (device)
+ *   k, v    : bf16 [B, H, Nk, 128] (device)
+ *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i
+ *             (both counted from 0)
+ *   out     : fp32 [B, H, Nq, 128] (device, written)
+ * Nq = 0 (or B*H = 0) is a no-op; Nk = 0 with Nq > 0 is MXATTN_ERR_INVALID_ARG
+ * (a softmax over no keys). The sizes obey the limits of mxattn_forward. */
+MXATTN_API mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H,
+                                             int64_t Nq, int64_t Nk, int64_t D, int causal, float* out, void* stream);
 
 /* Ablation variants ("MXAttention" section 5.4, Table 3): the same kernels
  * with the scale rule, the rotation and the placement of l as switches.

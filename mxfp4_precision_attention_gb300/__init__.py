@@ -69,7 +69,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mxattn_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
         lib.mxattn_forward_dump_phat.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P, P, P]
         lib.mxattn_forward_out_bf16.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, P]
-        lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P]
+        lib.mxattn_forward_bf16.argtypes = [P, P, P, I64, I64, I64, I64, I64, I, P, P]
         Dbl = ctypes.c_double
         lib.mxattn_quantize_qk_ex.argtypes = [P, I64, I64, I64, I64, I, Dbl, I, P, P, P]
         lib.mxattn_quantize_v_ex.argtypes = [P, I64, I64, I64, I64, I, Dbl, P, P, P]
@@ -350,12 +350,15 @@ def mxattn_forward_ex(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, v
 
 def mxattn_forward_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """BF16 tcgen05 attention forward (comparison path). Returns fp32 [B, H, N, 128]."""
-    B, H, N, Dx = _shape(q)
-    if _shape(k) != (B, H, N, Dx) or _shape(v) != (B, H, N, Dx):
-        raise ValueError("q, k and v must have the same shape")
-    out = _out(out, B, H, N, torch.float32, q.device)
-    _raise(load().mxattn_forward_bf16(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
+    """BF16 tcgen05 attention forward (comparison path): q [B, H, Nq, 128], k and v
+    [B, H, Nk, 128]; causal means key j is visible to query i iff j <= i.
+    Returns fp32 [B, H, Nq, 128]."""
+    B, H, Nq, Dx = _shape(q)
+    Nk = _shape(k)[2]
+    if _shape(k) != (B, H, Nk, Dx) or _shape(v) != (B, H, Nk, Dx):
+        raise ValueError("k and v must be [B, H, Nk, D] with q's B, H and D")
+    out = _out(out, B, H, Nq, torch.float32, q.device)
+    _raise(load().mxattn_forward_bf16(_ptr(q), _ptr(k), _ptr(v), B, H, Nq, Nk, Dx, int(causal), _ptr(out),
                                       _stream(stream)))
     return out
 

@@ -468,20 +468,24 @@ mxattn_status mxattn_nvfp4_forward_dump_phat(const void* q_codes, const void* q_
                       phat_codes, phat_scales, stream, kRuleUOS, placement, 7.25, q_amax, k_amax, v_amax);
 }
 
-mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t N,
-                                  int64_t D, int causal, float* out, void* stream) {
+mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, int64_t B, int64_t H, int64_t Nq,
+                                  int64_t Nk, int64_t D, int causal, float* out, void* stream) {
   t_err[0] = '\0';
   bool empty = false;
-  MX_TRY(check_shape(B, H, N, D, &empty));
+  if (Nk < 0) return fail(MXATTN_ERR_INVALID_ARG, "negative size (Nk=%lld)", (long long)Nk);
+  MX_TRY(check_shape(B, H, Nq, D, &empty));
   if (empty) return MXATTN_OK;
+  bool no_keys = false;
+  MX_TRY(check_shape(B, H, Nk, D, &no_keys));
+  if (no_keys) return fail(MXATTN_ERR_INVALID_ARG, "Nk=0 with Nq=%lld queries: softmax over no keys", (long long)Nq);
   MX_TRY(check_ptr(q, "q"));
   MX_TRY(check_ptr(k, "k"));
   MX_TRY(check_ptr(v, "v"));
   MX_TRY(check_ptr(out, "out"));
   if (causal != 0 && causal != 1) return fail(MXATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
-  const Range ro = rng(out, f32_bytes(B, H, N));
-  if (overlap(ro, rng(q, bf16_bytes(B, H, N))) || overlap(ro, rng(k, bf16_bytes(B, H, N))) ||
-      overlap(ro, rng(v, bf16_bytes(B, H, N))))
+  const Range ro = rng(out, f32_bytes(B, H, Nq));
+  if (overlap(ro, rng(q, bf16_bytes(B, H, Nq))) || overlap(ro, rng(k, bf16_bytes(B, H, Nk))) ||
+      overlap(ro, rng(v, bf16_bytes(B, H, Nk))))
     return fail(MXATTN_ERR_INVALID_ARG, "out overlaps an input");
   if (get_encoder() == nullptr) return fail(MXATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   if (device_status_ptr() == nullptr) return fail(MXATTN_ERR_CUDA, "device status word unavailable");
@@ -490,7 +494,8 @@ mxattn_status mxattn_forward_bf16(const void* q, const void* k, const void* v, i
   a.k = k;
   a.v = v;
   a.BH = B * H;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
   a.causal = causal;
   a.out = out;
   a.debug_flags = g_debug_flags;

@@ -8,7 +8,9 @@
 //   l   = diag(alpha) l + P 1     a 16-column MMA against a constant ones tile,
 //                                 so l sums exactly the bf16 P that enters O
 //
-// Same warp roles and bounded-wait discipline as the MXFP4 kernel.
+// Queries and keys may differ in length (Nq, Nk); causal means key j is
+// visible to query i iff j <= i. Same warp roles and bounded-wait discipline
+// as the MXFP4 kernel.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -53,8 +55,8 @@ constexpr uint32_t kTmemCols = 512;
 struct Params {
   float* out;
   int* status;
-  int64_t N;
-  int NT;
+  int64_t Nq, Nk;  // query and key/value lengths
+  int NTq, NTk;     // their 128-row tile counts
   int causal;
   uint32_t debug_flags;
   float score_scale_log2;
@@ -101,9 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int bh = static_cast<int>(p.bh_major ? blockIdx.x : blockIdx.y);
   const int slot = static_cast<int>(p.bh_major ? blockIdx.y : blockIdx.x);
-  const int qt = p.causal ? (p.NT - 1 - slot) : slot;  // causal: heaviest query tiles first
-  const int T = p.causal ? qt + 1 : p.NT;
-  const int64_t N = p.N;
+  const int qt = p.causal ? (p.NTq - 1 - slot) : slot;  // causal: heaviest query tiles first
+  // causal: key j is visible to query i iff j <= i (both counted from 0)
+  const int T = p.causal ? (qt + 1 < p.NTk ? qt + 1 : p.NTk) : p.NTk;
+  const int64_t Nq = p.Nq, Nk = p.Nk;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);
     float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
     const float C = p.score_scale_log2;
-    const bool ragged = (N % 128) != 0;
+    const bool ragged = (Nk % 128) != 0;
     float m_run = -INFINITY;
     bool my_abort = false, aborted = false;
     auto wait_uniform = [&](int b, uint32_t parity) {
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; i++) {
           const int64_t key = key0 + i;
-          if (!(key < N && (!p.causal || key <= qrow))) v[i] = -INFINITY;
+          if (!(key < Nk && (!p.causal || key <= qrow))) v[i] = -INFINITY;
         }
       }
       float pm = v[0];
@@ -332,12 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(2, 256);
     const float inv_l = 1.0f / lsum[r];
     if (!my_abort && !aborted) {
-      float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + qrow) * kD + 64 * h);
+      float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * Nq + qrow) * kD + 64 * h);
       for (int c = 0; c < 2; c++) {
         uint32_t rr[32];
-        tmem_ld32(tl + kColO + 64 * h + 32 * c, rr);  // warp-wide; rows past N load but do not store
+        tmem_ld32(tl + kColO + 64 * h + 32 * c, rr);  // warp-wide; rows past Nq load but do not store
         tmem_wait_ld();
-        if (qrow < N) {
+        if (qrow < Nq) {
 #pragma unroll
           for (int i = 0; i < 8; i++)
             dst[8 * c + i] = make_float4(__uint_as_float(rr[4 * i]) * inv_l, __uint_as_float(rr[4 * i + 1]) * inv_l,
@@ -359,20 +362,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s) {
-  const int64_t N = a.N, BH = a.BH;
-  const int64_t NT = ceil_div(N, 128);
+  const int64_t Nq = a.Nq, Nk = a.Nk, BH = a.BH;
+  const int64_t NTq = ceil_div(Nq, 128), NTk = ceil_div(Nk, 128);
   alignas(64) CUtensorMap tq, tk, tv;
-  const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
-  const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(N) * kD * 2};
+  const uint64_t dq[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Nq), static_cast<uint64_t>(BH)};
+  const uint64_t sq[2] = {kD * 2, static_cast<uint64_t>(Nq) * kD * 2};
+  const uint64_t dk[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Nk), static_cast<uint64_t>(BH)};
+  const uint64_t sk[2] = {kD * 2, static_cast<uint64_t>(Nk) * kD * 2};
   const uint32_t box[3] = {64, 128, 1};
-  if (!encode_tensor_map(&tq, 1, 3, const_cast<void*>(a.q), dims, strides, box, 128)) return cudaErrorInvalidValue;
-  if (!encode_tensor_map(&tk, 1, 3, const_cast<void*>(a.k), dims, strides, box, 128)) return cudaErrorInvalidValue;
-  if (!encode_tensor_map(&tv, 1, 3, const_cast<void*>(a.v), dims, strides, box, 128)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map(&tq, 1, 3, const_cast<void*>(a.q), dq, sq, box, 128)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map(&tk, 1, 3, const_cast<void*>(a.k), dk, sk, box, 128)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map(&tv, 1, 3, const_cast<void*>(a.v), dk, sk, box, 128)) return cudaErrorInvalidValue;
   Params p;
   p.out = a.out;
   p.status = device_status_ptr();
-  p.N = N;
-  p.NT = static_cast<int>(NT);
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.NTq = static_cast<int>(NTq);
+  p.NTk = static_cast<int>(NTk);
   p.causal = a.causal;
   p.debug_flags = a.debug_flags;
   p.score_scale_log2 = 1.4426950408889634f / 11.313708498984761f;
@@ -387,9 +394,9 @@ cudaError_t launch_bf16_forward(const Bf16FwdArgs& a, cudaStream_t s) {
     attr_set[dev] = true;
   }
   // causal: heads on x so that every head's longest query tile starts first
-  p.bh_major = (a.causal && NT <= 65535) ? 1 : 0;
-  dim3 grid = p.bh_major ? dim3(static_cast<unsigned>(BH), static_cast<unsigned>(NT))
-                         : dim3(static_cast<unsigned>(NT), static_cast<unsigned>(BH));
+  p.bh_major = (a.causal && NTq <= 65535) ? 1 : 0;
+  dim3 grid = p.bh_major ? dim3(static_cast<unsigned>(BH), static_cast<unsigned>(NTq))
+                         : dim3(static_cast<unsigned>(NTq), static_cast<unsigned>(BH));
   bf16_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

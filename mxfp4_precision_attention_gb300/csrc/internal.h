@@ -73,10 +73,10 @@ struct Mxfp4FwdArgs {
 cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s);
 
 struct Bf16FwdArgs {
-  const void* q;
-  const void* k;
-  const void* v;
-  int64_t BH, N;
+  const void* q;  // bf16 [BH][Nq][128]
+  const void* k;  // bf16 [BH][Nk][128]
+  const void* v;  // bf16 [BH][Nk][128]
+  int64_t BH, Nq, Nk;
   int causal;
   float* out;
   uint32_t debug_flags;

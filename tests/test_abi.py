@@ -71,8 +71,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.mxattn_quantize_v(odd, 1, 1, 128, 128, fake, fake, None) == 1
     assert "aligned" in _err(lib)
     # negative sizes, too many heads
-    assert lib.mxattn_forward_bf16(fake, fake, fake, 1, -1, 128, 128, 0, fake, None) == 1
-    assert lib.mxattn_forward_bf16(fake, fake, fake, 300, 300, 128, 128, 0, fake, None) == 2
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 1, -1, 128, 128, 128, 0, fake, None) == 1
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 300, 300, 128, 128, 128, 0, fake, None) == 2
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 1, 1, 128, -1, 128, 0, fake, None) == 1
+    assert lib.mxattn_forward_bf16(fake, fake, fake, 1, 1, 128, 0, 128, 0, fake, None) == 1
+    assert "Nk=0" in _err(lib)
     # overlapping outputs
     a = ctypes.c_void_p(0x100000)
     assert lib.mxattn_rotate_quantize_qk(a, 1, 1, 128, 128, ctypes.c_void_p(0x100000 + 4096), fake, None) == 1
@@ -110,7 +113,8 @@ def test_empty_problem_is_a_no_op(lib):
     assert lib.mxattn_rotate_quantize_qk(None, 1, 1, 0, 128, None, None, None) == 0
     assert lib.mxattn_quantize_v(None, 0, 4, 100, 128, None, None, None) == 0
     assert lib.mxattn_forward(None, None, None, None, None, None, None, 1, 1, 0, 128, 1, None, None) == 0
-    assert lib.mxattn_forward_bf16(None, None, None, 1, 0, 10, 128, 0, None, None) == 0
+    assert lib.mxattn_forward_bf16(None, None, None, 1, 0, 10, 10, 128, 0, None, None) == 0
+    assert lib.mxattn_forward_bf16(None, None, None, 1, 1, 0, 10, 128, 0, None, None) == 0
     assert lib.mxattn_quantize_qkv(None, None, None, 1, 1, 0, 128, None, None, None, None, None, None, None) == 0
 
 

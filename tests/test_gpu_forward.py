@@ -393,3 +393,25 @@ def test_cuda_graph_capture_and_replay(mx, causal):
     torch.cuda.synchronize()
     assert torch.equal(out, mx.mxattn_attention(q2, k2, v2, causal=causal))
     mx.mxattn_check()
+
+
+@pytest.mark.parametrize("nq,nk,causal", [(300, 200, False), (200, 300, False), (300, 200, True), (200, 333, True),
+                                          (129, 1, False), (1, 257, True), (513, 384, True)])
+def test_bf16_forward_query_and_key_lengths_differ(mx, nq, nk, causal):
+    """BF16 path with Nq != Nk against float64 softmax attention (Eq. 1) on the
+    same bf16 inputs; causal keeps key j for query i iff j <= i. Bound as in
+    the equal-length test: one bf16 rounding of each P entry."""
+    w = W.WORKLOADS["lognormal_4096"]
+    q = W.generate(w, device="cuda", B=1, H=2, N=nq, seed=nq)[0]
+    _, k, v = W.generate(w, device="cuda", B=1, H=2, N=nk, seed=nk + 7)
+    out = mx.mxattn_forward_bf16(q, k, v, causal=causal)
+    mx.mxattn_check()
+    assert out.shape == (1, 2, nq, 128)
+    qd, kd, vd = (t.double().cpu() for t in (q, k, v))
+    s = qd @ kd.transpose(-1, -2) / 128 ** 0.5
+    if causal:
+        s = s.masked_fill(torch.arange(nk)[None, :] > torch.arange(nq)[:, None], float("-inf"))
+    ref = torch.softmax(s, -1) @ vd
+    err = (out.double().cpu() - ref).abs().max().item()
+    bound = 2 * 2 ** -9 * vd.abs().max().item()
+    assert err <= bound, (err, bound)
