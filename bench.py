@@ -172,7 +172,7 @@ def cpu_oracle_sample(w, budget_rows: int, seed: int = 0):
     """Time the oracle on a bounded sample of workload `w`: per sampled head, its
     K and V quantized in full plus up to N query rows through the forward, over
     as many heads as `budget_rows` needs. Returns (seconds, flops, description,
-    threads)."""
+    threads, rows)."""
     import numpy as np
 
     import oracle
@@ -206,7 +206,14 @@ def cpu_oracle_sample(w, budget_rows: int, seed: int = 0):
         rows_done += nr
     desc = (f"{nheads} head(s) of {w.name}: per head rotate+quantize the sampled Q rows and all {w.N} K tokens, "
             f"quantize all V, float64 forward for the sampled rows against all keys ({rows_done} rows in total)")
-    return dt, flops, desc, oracle.num_threads()
+    return dt, flops, desc, oracle.num_threads(), rows_done
+
+
+def cpu_extrapolation(w, seconds: float, flops: float, rows: int) -> dict:
+    """Rows per second of the sample and a linear extrapolation of the sample's
+    rate (FLOP per second) to the whole workload."""
+    return {"rows_per_s": rows / seconds, "extrapolated_full_workload_s": w.flops / (flops / seconds),
+            "extrapolation": "linear in FLOP from the sample's rate"}
 
 
 def run_reference(args, w):
@@ -214,16 +221,17 @@ def run_reference(args, w):
     if rank != 0:
         return
     # calibrate the sample so that one step costs ~ args.ref_step_s seconds
-    dt, fl, _, _ = cpu_oracle_sample(w, 256)
+    dt, fl, _, _, _ = cpu_oracle_sample(w, 256)
     per_row = max(dt / 256, 1e-6)
     rows = int(max(8, min(200000, args.ref_step_s / per_row)))
     for i in range(args.warmup):
         cpu_oracle_sample(w, max(4, rows // 8), seed=100 + i)
-    times, flops = [], []
+    times, flops, nrows = [], [], 0
     for i in range(args.steps):
-        dt, fl, desc, thr = cpu_oracle_sample(w, rows, seed=i)
+        dt, fl, desc, thr, nr = cpu_oracle_sample(w, rows, seed=i)
         times.append(dt)
         flops.append(fl)
+        nrows += nr
     total_t, total_f = sum(times), sum(flops)
     value = total_f / total_t / 1e12
     line = {
@@ -232,7 +240,8 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": 128, "causal": w.causal,
                    "sample_rows_per_step": rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
+                         **cpu_extrapolation(w, total_t, total_f, nrows)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -460,11 +469,11 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        dt0, _, _, _ = cpu_oracle_sample(w, 256)
+        dt0, _, _, _, _ = cpu_oracle_sample(w, 256)
         rows = int(max(8, min(200000, args.cpu_budget_s / max(dt0 / 256, 1e-6))))
-        dt, fl, desc, thr = cpu_oracle_sample(w, rows, seed=1)
+        dt, fl, desc, thr, nr = cpu_oracle_sample(w, rows, seed=1)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+               "seconds": dt, **cpu_extrapolation(w, dt, fl, nr)}
 
     if rank == 0:
         line = {
