@@ -96,10 +96,13 @@ constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2 groups]: S holds S_g of 
 constexpr int kBarSEmpty = kBarSFull + 2;         // 4 arrivals: the S buffer was read
 constexpr int kBarPFull = kBarSEmpty + 1;         // [2 groups], 4 arrivals: P^ tile + O rescale ready
 constexpr int kBarODone = kBarPFull + 2;          // [2 groups]: P^V^ into O_g complete
-constexpr int kBarDiagV = kBarODone + 2;          // causal: the diagonal tile's bf16 V landed (group A, then B)
-constexpr int kBarDiagP = kBarDiagV + 1;          // [2 groups], 4 arrivals: the group's bf16 P^ rows written
+constexpr int kBarDiagV = kBarODone + 2;          // [2 groups] causal: the group's diagonal bf16 V tile landed
+constexpr int kBarDiagP = kBarDiagV + 2;          // [2 groups], 4 arrivals: the group's bf16 P^ rows written
 constexpr int kBarDiagDone = kBarDiagP + 2;       // [2 groups]: the diagonal product into O_g complete
 static_assert(kBarDiagDone + 2 <= kNumBars, "barrier space");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kKStages * kTileBytes >= 32768 &&
+                  kVStages * kVTileBytes >= 32768,
+              "the rings hold group B's diagonal operands (128-byte swizzle, 32 KB each)");
 
 // TMEM columns
 constexpr uint32_t kColS = 0;
@@ -291,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarSEmpty), 4);
     if constexpr (kDiagMma) {
-      mbar_init(bar(kBarDiagV), 1);
       for (int g = 0; g < 2; g++) {
+        mbar_init(bar(kBarDiagV + g), 1);
         mbar_init(bar(kBarDiagP + g), 4);
         mbar_init(bar(kBarDiagDone + g), 1);
       }
@@ -882,16 +885,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // own 32-key block (zero beyond the row and outside the block; exact in
           // bf16, an E2M1 value times a power of two) times the diagonal tile's
           // bf16 V rows, one kind::f16 128x128x128 product accumulated into O_g
-          // after its last P^V^. Both groups share one 64 KB region, group A (the
-          // earlier diagonal) first; every wait is bounded.
-          const uint32_t vdiag = sb + kOffDiag;          // [channels 0-63 | 64-127][128 keys][128 B]
-          uint8_t* pdiag = smem + kOffDiag + 32768;      // [keys 0-63 | 64-127][128 rows][128 B]
+          // after its last P^V^; every wait is bounded. Group A uses its own
+          // 64 KB region. Group B's operands go to the K ring (its V) and the V
+          // ring (its P^): B's epilogue starts once its last P^V^ is complete, and
+          // every QK^T and P^V^ that read the rings completed before that one.
+          const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
+          uint8_t* pdiag = g ? smem + kOffV : smem + kOffDiag + 32768;  // [keys 0-63 | 64-127][128 rows][128 B]
           const bool leader = quad == 0 && lane == 0;
-          if (g == 1) wait_uniform(kBarDiagDone + 0, 0);  // group A's product has read the region
           if (leader && !my_abort) {
-            mbar_arrive_expect_tx(bar(kBarDiagV), 32768);
-            tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV), 0, (Tg - 1) * kTile, bh);
-            tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV), 64, (Tg - 1) * kTile, bh);
+            mbar_arrive_expect_tx(bar(kBarDiagV + g), 32768);
+            tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV + g), 0, (Tg - 1) * kTile, bh);
+            tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV + g), 64, (Tg - 1) * kTile, bh);
           }
           if constexpr (kNv) {
             // O_g holds V^'s encoded units (x e_tV): bring this row to real units
@@ -945,11 +949,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar(kBarDiagP + g));
           if (leader) {
             bool ok = !my_abort && mbar_wait(bar(kBarDiagP + g), 0, abort_flag) &&
-                      mbar_wait(bar(kBarDiagV), g, abort_flag);
+                      mbar_wait(bar(kBarDiagV + g), 0, abort_flag);
             if (ok) {
               tc_fence_after();
               const uint32_t idd = idesc_bf16(128, 128, true);
-              const uint32_t pa = sb + kOffDiag + 32768;
+              const uint32_t pa = smem_u32(pdiag);
               for (int i = 0; i < 8; i++)
                 mma_bf16(tmem + ocol, smem_desc(pa + (i >> 2) * 16384 + (i & 3) * 32, 16, 1024, kSwizzle128B),
                          smem_desc(vdiag + i * 2048, 16384, 1024, kSwizzle128B), idd, 1u);
