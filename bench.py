@@ -41,9 +41,9 @@ NOMINAL_FP4_TFLOPS = 13500.0  # nominal dense FP4 tensor rate of one GB300
 # of the kernel source it was taken on. `traffic` is reported (scaled by B*H)
 # only while the source still has that fingerprint; otherwise it is null.
 FWD_TRAFFIC_CAPTURE = {
-    "fingerprint": "cf2e3fa0440cf44e",
+    "fingerprint": "a14d0d2108a67d8a",
     "bh": 8, "n": 32760,
-    "read_bytes": 53567488, "write_bytes": 77231872,
+    "read_bytes": 53726208, "write_bytes": 76930816,
 }
 FWD_SOURCES = ("attn_mxfp4.cu", "sm103_ptx.cuh", "internal.h")
 
