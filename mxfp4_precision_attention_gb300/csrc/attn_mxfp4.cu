@@ -100,6 +100,8 @@ constexpr int kBarDiagV = kBarODone + 2;          // [2 groups] causal: the grou
 constexpr int kBarDiagP = kBarDiagV + 2;          // [2 groups], 4 arrivals: the group's bf16 P^ rows written
 constexpr int kBarDiagDone = kBarDiagP + 2;       // [2 groups]: the diagonal product into O_g complete
 static_assert(kBarDiagDone + 2 <= kNumBars, "barrier space");
+static_assert(kOffP % 1024 == 0 && kTileBytes % 2048 == 0,
+              "the epilogue's staging rows (2 KB per warp and half) are whole 128-byte-swizzle atoms");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kKStages * kTileBytes >= 32768 &&
                   kVStages * kVTileBytes >= 32768,
               "the rings hold group B's diagonal operands (128-byte swizzle, 32 KB each)");
@@ -244,7 +246,7 @@ template <bool kCausal, bool kDump, bool kVariant, bool kNv = false, bool kBf16O
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vb,
-                     const Params p) {
+                     const __grid_constant__ CUtensorMap tm_o, const Params p) {
   static_assert(!kNv || kVariant, "NVFP4 runs as a variant kernel");
   // causal: the diagonal block's P^ x bf16 V runs on the tensor cores
   constexpr bool kDiagMma = kCausal;
@@ -812,7 +814,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // each 32-column chunk goes through the warp's own rows of the group's
         // two P^ buffers (free: every P^V^ of the group has completed), rows
         // 0-15 in the first and 16-31 in the second, 16-byte units swizzled by
-        // row % 8; then each store instruction writes four rows' 128 bytes.
+        // row % 8 (the 128-byte swizzle of a TMA box). The non-causal kernels
+        // then store each half with one TMA copy (rows past N are clipped) and
+        // wait for it to read the staging rows before the next chunk; the
+        // causal kernels store four rows' 128 bytes per instruction.
         auto store_rows = [&](float inv) {
           uint8_t* stg0 = smem + kOffP + 2 * g * kTileBytes + quad * 2048;
           uint8_t* stg1 = stg0 + kTileBytes;
@@ -841,15 +846,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 4; i < 8; i++)
                   *reinterpret_cast<uint4*>(mine + ((i ^ (lane & 7)) << 4)) = pk(o2 + 8 * (i - 4));
               }
-              __syncwarp();
+              if constexpr (!kCausal) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  if (row0 < N) tma_store_3d(&tm_o, smem_u32(stg0), 128 * c, static_cast<int>(row0), bh);
+                  if (row0 + 16 < N) tma_store_3d(&tm_o, smem_u32(stg1), 128 * c, static_cast<int>(row0 + 16), bh);
+                  bulk_commit_group();
+                  bulk_wait_group_read0();
+                }
+                __syncwarp();
+              } else {
+                __syncwarp();
 #pragma unroll
-              for (int it = 0; it < 8; it++) {
-                const int i = 4 * it + (lane >> 3), u = lane & 7;
-                const uint4 val = *reinterpret_cast<const uint4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
-                if (row0 + i < N)
-                  reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 64 * c)[u] = val;
+                for (int it = 0; it < 8; it++) {
+                  const int i = 4 * it + (lane >> 3), u = lane & 7;
+                  const uint4 val = *reinterpret_cast<const uint4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
+                  if (row0 + i < N)
+                    reinterpret_cast<uint4*>(p.out_bf16 + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 64 * c)[u] = val;
+                }
+                __syncwarp();
               }
-              __syncwarp();
             }
           } else {
 #pragma unroll 1
@@ -866,15 +883,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                       make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                   __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
               }
-              __syncwarp();
+              if constexpr (!kCausal) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  if (row0 < N) tma_store_3d(&tm_o, smem_u32(stg0), 128 * c, static_cast<int>(row0), bh);
+                  if (row0 + 16 < N) tma_store_3d(&tm_o, smem_u32(stg1), 128 * c, static_cast<int>(row0 + 16), bh);
+                  bulk_commit_group();
+                  bulk_wait_group_read0();  // the staging rows are rewritten by the next chunk
+                }
+                __syncwarp();
+              } else {
+                __syncwarp();
 #pragma unroll
-              for (int it = 0; it < 8; it++) {
-                const int i = 4 * it + (lane >> 3), u = lane & 7;
-                const float4 val = *reinterpret_cast<const float4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
-                if (row0 + i < N)
-                  reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 32 * c)[u] = val;
+                for (int it = 0; it < 8; it++) {
+                  const int i = 4 * it + (lane >> 3), u = lane & 7;
+                  const float4 val = *reinterpret_cast<const float4*>((i < 16 ? stg0 : stg1) + (i & 15) * 128 + ((u ^ (i & 7)) << 4));
+                  if (row0 + i < N)
+                    reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(bh) * N + row0 + i) * kD + 32 * c)[u] = val;
+                }
+                __syncwarp();  // the staging rows are rewritten by the next chunk
               }
-              __syncwarp();  // the staging rows are rewritten by the next chunk
             }
           }
         };
@@ -1137,6 +1166,16 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
     if (!encode_tensor_map(&tvb, 1, 3, const_cast<void*>(a.v_bf16), dims, strides, box, 128))
       return cudaErrorInvalidValue;
   }
+  alignas(64) CUtensorMap to;
+  {
+    const bool ob = a.out_bf16 != nullptr;
+    const uint64_t row = ob ? kD * 2 : kD * 4;
+    const uint64_t dims[3] = {row, static_cast<uint64_t>(N), static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {row, static_cast<uint64_t>(N) * row};
+    const uint32_t box[3] = {128, 16, 1};
+    if (!encode_tensor_map(&to, 0, 3, ob ? a.out_bf16 : static_cast<void*>(a.out), dims, strides, box, 128))
+      return cudaErrorInvalidValue;
+  }
   Params p;
   p.q_scales = static_cast<const uint8_t*>(a.q_scales);
   p.k_scales = static_cast<const uint8_t*>(a.k_scales);
@@ -1209,27 +1248,27 @@ cudaError_t launch_mxfp4_forward(const Mxfp4FwdArgs& a, cudaStream_t s) {
   if (nv && (a.causal == 2 || a.p_rule != kRuleUOS)) return cudaErrorNotSupported;
   if (a.out_bf16 != nullptr) {  // bf16 output: the plain MXFP4 kernels only (UOS, PNQ, no dump)
     if (nv || variant || dump) return cudaErrorNotSupported;
-    if (a.causal) mxfp4_fwd_kernel<true, false, false, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
-    else mxfp4_fwd_kernel<false, false, false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
+    if (a.causal) mxfp4_fwd_kernel<true, false, false, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, to, p);
+    else mxfp4_fwd_kernel<false, false, false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, to, p);
     return cudaGetLastError();
   }
   if (nv) {
     if (a.causal) {
-      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, p);
-      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, p);
+      if (dump) mxfp4_fwd_kernel<true, true, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, to, p);
+      else mxfp4_fwd_kernel<true, false, true, true><<<grid, kThreads, kSmemNvC, s>>>(tq, tk, tv, tvb, to, p);
     } else {
-      if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
-      else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, p);
+      if (dump) mxfp4_fwd_kernel<false, true, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, to, p);
+      else mxfp4_fwd_kernel<false, false, true, true><<<grid, kThreads, kSmemNv, s>>>(tq, tk, tv, tvb, to, p);
     }
   } else if (variant) {
-    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
-    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
+    if (a.causal) mxfp4_fwd_kernel<true, false, true><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, to, p);
+    else mxfp4_fwd_kernel<false, false, true><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, to, p);
   } else if (a.causal) {
-    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
-    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, p);
+    if (dump) mxfp4_fwd_kernel<true, true, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, to, p);
+    else mxfp4_fwd_kernel<true, false, false><<<grid, kThreads, kSmemMxC, s>>>(tq, tk, tv, tvb, to, p);
   } else {
-    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
-    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, p);
+    if (dump) mxfp4_fwd_kernel<false, true, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, to, p);
+    else mxfp4_fwd_kernel<false, false, false><<<grid, kThreads, kSmemMx, s>>>(tq, tk, tv, tvb, to, p);
   }
   return cudaGetLastError();
 }
