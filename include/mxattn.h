@@ -255,7 +255,8 @@ MXATTN_API size_t mxattn_workspace_bytes(int64_t B, int64_t H, int64_t N);
  * the kernels) into `workspace` (device, >= mxattn_workspace_bytes, 256-byte
  * aligned), runs mxattn_quantize_qkv and mxattn_forward, copies the fp32 result to out_host, and synchronizes
  * `stream` before returning, so out_host is ready on MXATTN_OK.
- * The B*H heads run as up to 16 chunks: each chunk's copy in, kernels and
+ * The B*H heads run in chunks (the first and the last of one head, the
+ * others of about 52 MB of input each, at most 64): each chunk's copy in, kernels and
  * copy out are ordered by events, with the copies on two internal streams
  * and the kernels alternating between `stream` and a third internal stream
  * (all created on the first call on a device and kept). The copies start

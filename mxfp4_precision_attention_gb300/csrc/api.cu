@@ -183,7 +183,12 @@ mxattn_status forward_impl(const void* qc, const void* qs, const void* kc, const
 // Internal copy streams and events of mxattn_attention_host, created once per
 // device and reused; a call holds the device's lock while it enqueues and
 // waits, so concurrent host calls on one device run one after the other.
-constexpr int64_t kHostChunks = 16;
+constexpr int64_t kHostChunks = 64;  // at most this many chunks (events per direction)
+// Input bytes (bf16 Q, K and V) per middle chunk. Smaller chunks add per-chunk
+// launch and synchronisation gaps; larger ones lengthen the pipeline's fill
+// and drain. Measured best at 50-57 MB on GB300 for both the Wan-shaped
+// (compute-bound) and the causal 8192-token (copy-bound) workloads.
+constexpr size_t kHostChunkBytes = size_t(52) << 20;
 struct HostPipe {
   std::mutex mu;
   cudaStream_t h2d = nullptr, d2h = nullptr, alt = nullptr;
@@ -551,24 +556,26 @@ mxattn_status mxattn_attention_host(const void* q_host, const void* k_host, cons
   if (hp == nullptr) return cuda_fail(e, "host copy streams");
   std::lock_guard<std::mutex> lock(hp->mu);
   const int64_t BH = B * H;
+  const int64_t NT = ceil_div(N, kTile), npad_half = ceil_div(N, kBlock) * kBlock / 2;
+  const size_t xh = static_cast<size_t>(N) * kD * 2, oh = static_cast<size_t>(N) * kD * 4;
   // Chunk boundaries: the first and the last chunk hold one head, so the
   // kernels start after a short copy and the final copy out is short; the
-  // heads in between are spread evenly over the remaining chunks.
+  // heads in between go in chunks of about kHostChunkBytes of input.
   int64_t bounds[kHostChunks + 1];
   int64_t nchunks = 0;
   {
     const int64_t edge = BH >= 4 ? 1 : 0;
     const int64_t mid_heads = BH - 2 * edge;
-    const int64_t mid_chunks = mid_heads < kHostChunks - 2 * edge ? mid_heads : kHostChunks - 2 * edge;
-    const int64_t per = ceil_div(mid_heads, mid_chunks);
+    const size_t head_in = 3 * xh;
+    int64_t per = static_cast<int64_t>((kHostChunkBytes + head_in / 2) / head_in);
+    if (per < 1) per = 1;
+    if (ceil_div(mid_heads, per) > kHostChunks - 2 * edge) per = ceil_div(mid_heads, kHostChunks - 2 * edge);
     bounds[0] = 0;
     if (edge) bounds[++nchunks] = 1;
     for (int64_t h = edge + per; h < BH - edge; h += per) bounds[++nchunks] = h;
     if (edge) bounds[++nchunks] = BH - 1;
     bounds[++nchunks] = BH;
   }
-  const int64_t NT = ceil_div(N, kTile), npad_half = ceil_div(N, kBlock) * kBlock / 2;
-  const size_t xh = static_cast<size_t>(N) * kD * 2, oh = static_cast<size_t>(N) * kD * 4;
   const size_t qch = static_cast<size_t>(N) * 64, sfh = static_cast<size_t>(NT) * kSfAtomBytes,
                vch = static_cast<size_t>(kD) * npad_half;
   // copies into the workspace may start once earlier work on `stream` is done

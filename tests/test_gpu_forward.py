@@ -257,13 +257,14 @@ def test_device_convenience_call_matches_device_path(mx, causal):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_host_entry_point_pipelined_chunks(mx, causal):
-    """21 heads run as 16 chunks (one head in the first and in the last) whose
+    """21 heads of 32760 tokens (25 MB of input per head) run as 12 chunks
+    (one head in the first and in the last, two in each of the others) whose
     copies overlap the kernels; two calls in a row (the internal streams and
     events are reused) give the device path's output bit for bit."""
-    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=3, H=7, N=300, seed=17)
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=3, H=7, N=32760, seed=17)
     dev = _gpu_mx(mx, q, k, v, causal=causal).cpu()
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    ws = torch.empty(mx.mxattn_workspace_bytes(3, 7, 300), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(mx.mxattn_workspace_bytes(3, 7, 32760), dtype=torch.uint8, device="cuda")
     for _ in range(2):
         outh = torch.full(q.shape, float("nan"), dtype=torch.float32).pin_memory()
         mx.mxattn_attention_host(qh, kh, vh, causal, outh, ws)
