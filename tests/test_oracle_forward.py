@@ -223,3 +223,65 @@ def test_forward_on_codes_matches_real_valued_core(orc):
     for r, (bh, i) in enumerate(rows):
         ref = orc.online_softmax(Q[bh, i][None], [i], Kd[bh], Vd[bh], quant_p=True)
         assert np.array_equal(res["out"][r], ref["out"][0])
+
+
+# ------------------------------------------------------------ Eq. (1) oracle
+def _bf16(x):
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_vals(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 33, 129, 300])
+def test_sdpa_is_softmax_attention(orc, causal, N):
+    """orc.sdpa is Eq. (1) of section 2: softmax(QK^T / sqrt(d)) V on the bf16
+    inputs, keys j <= i only when causal. Compared with a numpy evaluation of
+    the same formula on every row of a ragged N, causal and not."""
+    rng = np.random.default_rng(100 + N)
+    BH = 2
+    q = _bf16(rng.standard_normal((BH, N, D)) * 2)
+    k = _bf16(rng.standard_normal((BH, N, D)))
+    v = _bf16(rng.standard_normal((BH, N, D)))
+    rows = np.array([[b, i] for b in range(BH) for i in range(N)], dtype=np.int64)
+    got = orc.sdpa(q, k, v, rows, causal=causal)
+    for b in range(BH):
+        Q, K, V = _bf16_vals(q[b]), _bf16_vals(k[b]), _bf16_vals(v[b])
+        ref = _softmax_attn(Q, K, V, np.arange(N) if causal else None)
+        assert np.max(np.abs(got[b * N:(b + 1) * N] - ref)) < 1e-12
+
+
+def test_sdpa_closed_forms(orc):
+    """Two closed forms of Eq. (1) that fail on a wrong 1/sqrt(d) or a shifted
+    causal mask: (i) equal keys give uniform weights, so row i of a causal
+    pass is the mean of V rows 0..i and of a full pass the mean of all rows;
+    (ii) with two keys whose scores differ by exactly sqrt(d) * ln 2 the
+    softmax weights are 2/3 and 1/3."""
+    N = 40
+    rng = np.random.default_rng(7)
+    q = _bf16(rng.standard_normal((1, N, D)))
+    k = _bf16(np.tile(rng.standard_normal((1, 1, D)), (1, N, 1)))
+    v = _bf16(rng.integers(-8, 9, (1, N, D)).astype(np.float32))
+    rows = np.array([[0, i] for i in range(N)], dtype=np.int64)
+    V = _bf16_vals(v[0])
+    causal = orc.sdpa(q, k, v, rows, causal=True)
+    full = orc.sdpa(q, k, v, rows, causal=False)
+    for i in range(N):
+        assert np.allclose(causal[i], V[: i + 1].mean(axis=0), rtol=0, atol=1e-12)
+        assert np.allclose(full[i], V.mean(axis=0), rtol=0, atol=1e-12)
+    # q . k0 - q . k1 = sqrt(128) ln 2 needs non-bf16 values; scale instead: q = e_0,
+    # k0 = a e_0, k1 = 0 with a = sqrt(128) ln 2 rounded to bf16, weights e^s / (e^s + 1)
+    a = float(_bf16_vals(_bf16(np.array([np.sqrt(D) * np.log(2.0)])))[0])
+    qq = np.zeros((1, 2, D)); qq[0, :, 0] = 1.0
+    kk = np.zeros((1, 2, D)); kk[0, 0, 0] = a
+    vv = np.zeros((1, 2, D)); vv[0, 0, :] = 3.0; vv[0, 1, :] = -6.0
+    out = orc.sdpa(_bf16(qq), _bf16(kk), _bf16(vv), np.array([[0, 1]]), causal=False)
+    w0 = np.exp(a / np.sqrt(D)) / (np.exp(a / np.sqrt(D)) + 1.0)
+    assert abs(w0 - 2.0 / 3.0) < 1e-2
+    assert np.allclose(out[0], 3.0 * w0 - 6.0 * (1.0 - w0), rtol=0, atol=1e-12)
+    # row 0 of a causal pass sees only key 0
+    out0 = orc.sdpa(_bf16(qq), _bf16(kk), _bf16(vv), np.array([[0, 0]]), causal=True)
+    assert np.allclose(out0[0], 3.0, rtol=0, atol=0)

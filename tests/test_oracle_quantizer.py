@@ -185,3 +185,46 @@ def test_ceil_q_rule_defines_the_qmax_sweep(orc):
     for m in M[:20000:7]:
         assert orc.scale_exponent(m, orc.CEIL_Q, 7.25) == orc.scale_exponent(m, orc.UOS)
         assert orc.scale_exponent(m, orc.CEIL_Q, 6.0) == orc.scale_exponent(m, orc.TFS)
+
+
+def test_rotate_then_quantize_composition(orc):
+    """Algorithm 2's Q/K steps in order: rotate each token with R_H (the pinned
+    binary32 butterfly, orc.hadamard_fp32), then Algorithm 1 on each 32-channel
+    block of the rotated row. orc.rotate_quantize_qk(rotate=True) must equal that
+    composition code for code and scale for scale, assembled here from the
+    separately pinned pieces (scale exponent, E2M1 code)."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((24, 128)) * np.exp2(rng.integers(-6, 6, (24, 1)))
+    x[3] = 0.0                                  # all-zero row: every block sigma = 1
+    x[4, :] = 0.0; x[4, 17] = 5.0               # one-hot rows rotate to +-5/sqrt(128)
+    bits = _bf16_bits(x)
+    codes, scales = orc.rotate_quantize_qk(bits, rotate=True)
+    y = orc.hadamard_fp32(bits).astype(np.float64)
+    for r in range(x.shape[0]):
+        for b in range(4):
+            blk = y[r, 32 * b: 32 * b + 32]
+            M = np.abs(blk).max()
+            if M == 0:
+                assert scales[r, b] == 127 and np.all(codes[r, 32 * b: 32 * b + 32] == 0)
+                continue
+            e = orc.scale_exponent(M, orc.UOS)
+            assert scales[r, b] == e + 127
+            ref = orc.e2m1_code(blk / 2.0 ** e)
+            assert np.array_equal(codes[r, 32 * b: 32 * b + 32], ref)
+    # without the rotation the same rows give different codes (the branch is live)
+    c0, _ = orc.rotate_quantize_qk(bits, rotate=False)
+    assert not np.array_equal(c0, codes)
+
+
+def test_rotated_basis_vectors_exact(orc):
+    """Integer inputs whose rotation is exact: x = e_j rotates to the j-th row of
+    H_128 times fl32(2^-3.5), entries +-0.0883883..., so every block maximum is
+    that value, e = ceil(log2(0.08839 / 7.25)) = -6 (scale byte 121), and every
+    element is +-5.657 in scale units, saturating to code 7 (6.0) with the sign
+    of (-1)^popcount(i & j) (the Sylvester entry, section 4.3 rotation)."""
+    for j in (0, 1, 5, 64, 127):
+        x = np.zeros((1, 128)); x[0, j] = 1.0
+        codes, scales = orc.rotate_quantize_qk(_bf16_bits(x), rotate=True)
+        assert np.all(scales == 121)
+        signs = np.array([bin(i & j).count("1") & 1 for i in range(128)])
+        assert np.array_equal(codes[0], (7 | (signs << 3)).astype(np.uint8))
