@@ -278,8 +278,13 @@ MXATTN_API mxattn_status mxattn_attention_host(const void* q_host, const void* k
  * that uses the library until the process exits; problems needing more
  * return MXATTN_ERR_UNSUPPORTED before anything is launched (B*H*N up to about
  * 160 000 token-heads fits). The entry point itself calls no allocator.
+ * q, k, v and out must be device memory of the current device (checked with
+ * cudaPointerGetAttributes before anything is launched; else
+ * MXATTN_ERR_INVALID_ARG).
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture. All calls
+ * device current; make that first call before any stream capture. The address
+ * is kept for the life of the device's primary context: do not call this
+ * entry point on a device after cudaDeviceReset of that device. All calls
  * share the array and it keeps the last call's contents (nothing in it needs
  * clearing: each call rewrites every byte it reads); calls that overlap on the
  * GPU (different streams without ordering, or several host threads) race on

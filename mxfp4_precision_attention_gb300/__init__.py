@@ -390,6 +390,11 @@ def mxattn_attention_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     B, H, N, Dx = _shape(q)
     if _shape(k) != (B, H, N, Dx) or _shape(v) != (B, H, N, Dx):
         raise ValueError("q, k and v must have the same shape")
+    if q.device.index != torch.cuda.current_device():
+        raise ValueError(f"q is on {q.device} but the current device is cuda:{torch.cuda.current_device()}; "
+                         "the library's scratch and launches belong to the current device")
+    _buf(k, 0, "k", q.device)
+    _buf(v, 0, "v", q.device)
     _buf(out, 4 * _elems(B, H, N), "out", q.device, torch.float32)
     _raise(load().mxattn_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), B, H, N, Dx, int(causal), _ptr(out),
                                            _stream(stream)))

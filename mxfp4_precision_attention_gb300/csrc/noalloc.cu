@@ -30,7 +30,10 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device. In host code the
 // symbol is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached. The cached address is valid
+// for the life of the device's primary context: after cudaDeviceReset the
+// module is loaded again, possibly elsewhere, so a process that resets a
+// device must not call this entry point on it again.
 uint8_t* scratch_on_current_device(cudaError_t* err) {
   static uint8_t* addr[64] = {nullptr};
   static std::mutex mu;
@@ -53,6 +56,17 @@ uint8_t* scratch_on_current_device(cudaError_t* err) {
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// q, k, v and out must be device memory of the current device: the kernels run
+// there and would otherwise read another GPU's memory without peer access.
+bool on_current_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error left by an unknown pointer
+    return false;
+  }
+  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
+}
+
 }  // namespace
 
 size_t noalloc_scratch_needed(int64_t B, int64_t H, int64_t N) {
@@ -72,7 +86,16 @@ extern "C" mxattn_status mxattn_attention_noalloc(const void* q, const void* k, 
     set_last_error("mxattn_attention_noalloc: negative size");
     return MXATTN_ERR_INVALID_ARG;
   }
+  if (D != kD) {
+    set_last_error("mxattn_attention_noalloc: head dimension must be 128");
+    return MXATTN_ERR_UNSUPPORTED;
+  }
   if (B == 0 || H == 0 || N == 0) return MXATTN_OK;
+  // the same bounds as every other entry point, before any size product is formed
+  if (B > 65535 || H > 65535 || B * H > 65535 || N >= (int64_t(1) << 31) - kTile) {
+    set_last_error("mxattn_attention_noalloc: B*H must be at most 65535 and N below 2^31 - 128");
+    return MXATTN_ERR_UNSUPPORTED;
+  }
   const size_t need = noalloc_scratch_needed(B, H, N);
   if (need > kScratchBytes) {
     char msg[256];
@@ -82,6 +105,16 @@ extern "C" mxattn_status mxattn_attention_noalloc(const void* q, const void* k, 
              (long long)(B * H * N), need, kScratchBytes);
     set_last_error(msg);
     return MXATTN_ERR_UNSUPPORTED;
+  }
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) {
+    set_last_error("mxattn_attention_noalloc: q, k, v and out must be non-NULL");
+    return MXATTN_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !on_current_device(q, dev) || !on_current_device(k, dev) ||
+      !on_current_device(v, dev) || !on_current_device(out, dev)) {
+    set_last_error("mxattn_attention_noalloc: q, k, v and out must be device memory of the current device");
+    return MXATTN_ERR_INVALID_ARG;
   }
   cudaError_t e = cudaSuccess;
   uint8_t* s = scratch_on_current_device(&e);
