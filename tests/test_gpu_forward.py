@@ -142,6 +142,40 @@ def test_forward_full_size_sampled(mx, orc, name, nrows):
     _gate(g, ref["out"], f"{name} sampled")
 
 
+@pytest.mark.parametrize("name,nrows", [("wan_32760", 40), ("hunyuan_118800", 16)])
+def test_phat_flip_rate_full_length(mx, orc, name, nrows):
+    """The P^ gate at the full sequence length of the outlier workloads: one head of
+    the workload's recipe (x20 outlier channels, near-one-hot rows) at its full N,
+    every P^ tile of the sampled rows dumped and compared entry by entry with the
+    oracle's P^ (PNQ, Eqs. 44-48), and those rows' outputs within the tolerance.
+    The dump is the production kernel plus stores: its output must equal the
+    plain forward's bit for bit."""
+    w = W.WORKLOADS[name]
+    q, k, v = W.generate(w, device="cuda", H=1)
+    B, H, N = 1, 1, w.N
+    out, pc, ps = _gpu_mx(mx, q, k, v, causal=w.causal, dump=True)
+    plain = _gpu_mx(mx, q, k, v, causal=w.causal)
+    assert torch.equal(out, plain)
+    rng = np.random.default_rng(17)
+    tok = np.concatenate([rng.integers(0, N, nrows - 4), [0, 127, N - 1, (N - 1) // 128 * 128]])
+    rows = np.array([[0, int(i)] for i in tok], dtype=np.int64)
+    ridx = torch.tensor(rows[:, 1], device="cuda")
+    pcr = pc.reshape(N, -1).index_select(0, ridx).cpu().numpy()
+    psr = ps.reshape(N, -1).index_select(0, ridx).cpu().numpy()
+    g = out.reshape(N, 128).index_select(0, ridx).cpu().numpy().astype(np.float64)
+    del pc, ps, out, plain
+    torch.cuda.empty_cache()
+    ref = _oracle(orc, q, k, v, rows, causal=w.causal, want_phat=True)
+    vals = np.array([orc.e2m1_value(c) for c in range(16)])
+    gp = L.phat_values(pcr, psr, vals)
+    valid = np.broadcast_to(np.arange(gp.shape[1])[None, :] < N, gp.shape)
+    diff = (gp != ref["phat"]) & valid
+    rate = diff.sum() / valid.sum()
+    print(f"{name} full length: P^ flip rate {rate:.2e} ({diff.sum()} of {valid.sum()} entries)")
+    assert rate < MAX_FLIP_RATE
+    _gate(g, ref["out"], f"{name} full length, dumped rows")
+
+
 def test_causal_no_future_leakage_gpu(mx):
     q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=2, N=600, seed=31)
     base = _gpu_mx(mx, q, k, v, causal=True).clone()
