@@ -37,13 +37,15 @@ NOMINAL_FP4_TFLOPS = 13500.0  # nominal dense FP4 tensor rate of one GB300
 
 
 # DRAM bytes of one forward launch from an ncu capture (dram__bytes_read.sum,
-# dram__bytes_write.sum), with the B*H and N it was taken at and a fingerprint
-# of the kernel source it was taken on. `traffic` is reported (scaled by B*H)
-# only while the source still has that fingerprint; otherwise it is null.
+# dram__bytes_write.sum) of the full Wan-shaped launch (B*H = 40, N = 32760;
+# the 671 MB fp32 output is 5x the L2, so at most the L2's dirty residue at
+# exit goes uncounted), with a fingerprint of the kernel source it was taken
+# on. `traffic` is reported (scaled by B*H) only while the source still has
+# that fingerprint; otherwise it is null.
 FWD_TRAFFIC_CAPTURE = {
     "fingerprint": "854a4d3a9f1f7177",
-    "bh": 8, "n": 32760,
-    "read_bytes": 53519360, "write_bytes": 76665856,
+    "bh": 40, "n": 32760,
+    "read_bytes": 267590144, "write_bytes": 613803264,
 }
 FWD_SOURCES = ("attn_mxfp4.cu", "sm103_ptx.cuh", "internal.h")
 
@@ -65,10 +67,19 @@ def kernel_fingerprint() -> str:
 
 
 def fwd_traffic(bh: int, n: int):
+    """(read, write) DRAM bytes of one forward launch at B*H = bh, N = n, from the
+    capture above, or None if the kernel source or N differs from the capture's."""
     c = FWD_TRAFFIC_CAPTURE
     if c["fingerprint"] != kernel_fingerprint() or n != c["n"]:
         return None
-    return (c["read_bytes"] + c["write_bytes"]) * bh / c["bh"]
+    return c["read_bytes"] * bh / c["bh"], c["write_bytes"] * bh / c["bh"]
+
+
+def fwd_algorithmic_bytes(bh: int, n: int, out_bytes: int = 4) -> int:
+    """The forward's own bytes: Q^, K^, V^ codes and scale atoms read once, O written once."""
+    nt = (n + 127) // 128
+    codes = 2 * bh * n * 64 + bh * 128 * ((n + 31) // 32 * 32) // 2
+    return codes + 3 * bh * nt * 512 + bh * n * 128 * out_bytes
 
 
 def _peaks():
@@ -214,6 +225,57 @@ def cpu_extrapolation(w, seconds: float, flops: float, rows: int) -> dict:
     rate (FLOP per second) to the whole workload."""
     return {"rows_per_s": rows / seconds, "extrapolated_full_workload_s": w.flops / (flops / seconds),
             "extrapolation": "linear in FLOP from the sample's rate"}
+
+
+# The other seeded workloads, each timed in the same run as the headline line
+# (parity-test configurations, reported beside it; the tiny 512-token case is
+# launch-bound and left out).
+PER_WORKLOAD = ("lognormal_4096", "wan_32760", "hunyuan_118800", "causal_lm_8192")
+
+
+def time_workload(mx, W, w, stream, fp4_peak: float, hbm: float, cpu_s: float, reps: int = 5) -> dict:
+    """Forward and one-launch quantizer of workload `w`, CUDA events on `stream`
+    (3 warm-up launches, then the mean of `reps`), with its roofline fraction and,
+    if cpu_s > 0, the oracle timed on a bounded sample of the same workload."""
+    import torch
+
+    B, H, N = w.B, w.H, w.N
+    q, k, v = W.generate(w, device="cuda")
+    dev = q.device
+    qcn, qsn = mx.qk_layout_sizes(B, H, N)
+    vcn, vsn = mx.v_layout_sizes(B, H, N)
+    bufs = [torch.empty(n, dtype=torch.uint8, device=dev) for n in (qcn, qsn, qcn, qsn, vcn, vsn)]
+    out = torch.empty((B, H, N, 128), dtype=torch.float32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    with torch.cuda.stream(stream):
+        for rep in range(3 + reps):
+            if rep == 3: ev[0].record(stream)
+            mx.mxattn_quantize_qkv(q, k, v, out=tuple(bufs), stream=stream)
+        ev[1].record(stream)
+        for rep in range(3 + reps):
+            if rep == 3: ev[2].record(stream)
+            mx.mxattn_forward(*bufs, v, B, H, N, causal=w.causal, out=out, stream=stream)
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    mx.mxattn_check(stream)
+    q_ms = ev[0].elapsed_time(ev[1]) / reps
+    f_ms = ev[2].elapsed_time(ev[3]) / reps
+    e = B * H * N * 128
+    qb = 3 * e * 2 + 2 * (qcn + qsn) + vcn + vsn
+    tf = w.flops / (f_ms * 1e-3) / 1e12
+    res = {"B": B, "H": H, "N": N, "causal": w.causal, "forward_ms": f_ms, "tflops": tf, "frac": tf / fp4_peak,
+           "quantize_qkv_ms": q_ms, "quantizer_gbs": qb / (q_ms * 1e-3) / 1e9,
+           "quantizer_frac_of_hbm": qb / (q_ms * 1e-3) / 1e9 / hbm,
+           "step_tflops": w.flops / ((f_ms + q_ms) * 1e-3) / 1e12}
+    del q, k, v, bufs, out
+    torch.cuda.empty_cache()
+    if cpu_s > 0:
+        dt0, _, _, _, _ = cpu_oracle_sample(w, 64)
+        rows = int(max(8, min(200000, cpu_s / max(dt0 / 64, 1e-6))))
+        dt, fl, desc, thr, nr = cpu_oracle_sample(w, rows, seed=3)
+        res["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
+                               "sample": desc, "seconds": dt, **cpu_extrapolation(w, dt, fl, nr)}
+    return res
 
 
 def run_reference(args, w):
@@ -456,7 +518,7 @@ def run_ours(args, w):
         torch.cuda.empty_cache()
         ws = torch.empty(mx.mxattn_workspace_bytes(B, H, N), dtype=torch.uint8, device=dev)
         mx.mxattn_attention_host(qh, kh, vh, w.causal, outh, ws, stream=stream)
-        steps_e2e = max(1, min(args.steps, 3))
+        steps_e2e = max(1, args.steps)
         if world > 1:
             torch.distributed.barrier()
         t0 = time.perf_counter()
@@ -475,6 +537,16 @@ def run_ours(args, w):
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
                "seconds": dt, **cpu_extrapolation(w, dt, fl, nr)}
 
+    per_workload = None
+    if rank == 0 and not args.no_per_workload:
+        per_workload = {}
+        for pname in PER_WORKLOAD:
+            if pname == w.name:
+                continue
+            per_workload[pname] = time_workload(mx, W, W.WORKLOADS[pname], stream, fp4_peak, hbm,
+                                                cpu_s=0 if args.no_cpu_baseline else args.per_workload_cpu_s)
+
+    traffic = fwd_traffic(B * H, N)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -482,11 +554,18 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4",
             "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": 128, "causal": w.causal,
-                       "parallelism": f"replicas x{world} (heads shard, no collective)",
+                       "parallelism": (f"replicas x{world}: every rank runs the whole workload on its own seeded "
+                                       "inputs (weak scaling); no collective"),
                        "l2": f"inputs {3 * e * 2 / 1e9:.2f} GB per step vs 129 MB L2; no flush"},
             "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
-                         "frac": fwd_tflops / fp4_peak, "traffic": fwd_traffic(B * H, N),
-                         "traffic_note": "DRAM bytes per launch, scaled by B*H from an 8-head ncu capture of the same kernel source",
+                         "frac": fwd_tflops / fp4_peak,
+                         "traffic": None if traffic is None else traffic[0] + traffic[1],
+                         "traffic_read": None if traffic is None else traffic[0],
+                         "traffic_write": None if traffic is None else traffic[1],
+                         "algorithmic_bytes": fwd_algorithmic_bytes(B * H, N),
+                         "traffic_note": ("DRAM bytes per launch (ncu dram__bytes_read/write.sum of the full 40-head "
+                                          "launch of the same kernel source, scaled by B*H); writes still dirty in L2 "
+                                          "at kernel exit are not counted"),
                          "kernel": "mxfp4_fwd_kernel",
                          "peak_source": f"{peak_src} bf16 {bf16:.1f} TF/s x nominal fp4/bf16 ratio {FP4_OVER_BF16_NOMINAL:g}"},
             "breakdown_ms": {"quantize_qkv": qkv_ms, "forward": fwd_ms},
@@ -496,6 +575,7 @@ def run_ours(args, w):
                           "frac_of_hbm": qkv_bytes / (qkv_ms * 1e-3) / 1e9 / hbm, "hbm_peak": hbm,
                           "single_calls": single},
             "gpu_launches": 2 * args.steps,
+            "per_workload": per_workload,
             "bf16_path": bf16_path,
             "nvfp4_path": nvfp4_path,
             "fp4_mma_probe": mma_probe,
@@ -758,6 +838,8 @@ def main():
     ap.add_argument("--no-mma-probe", action="store_true", help="skip the dense FP4 MMA rate probe")
     ap.add_argument("--mma-probe-s", type=float, default=1.0, help="seconds of back-to-back MMAs in the probe")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--per-workload-cpu-s", type=float, default=6.0, help="oracle seconds per other workload")
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--accuracy", action="store_true",
                     help="accuracy of the ablation variants vs exact attention instead of timing")
