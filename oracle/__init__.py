@@ -87,6 +87,7 @@ def _load():
             lib.orc_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I, I, I, Dbl, I, I, P, I64, P, P, P, P]
             lib.orc_forward.restype = I
             lib.orc_sdpa.argtypes = [P, P, P, I64, I64, I, P, I64, P]
+            lib.orc_rowsum_parts.argtypes = [P, I64, I64, I, Dbl, P]
             lib.orc_e4m3_value.argtypes = [I]
             lib.orc_e4m3_value.restype = ctypes.c_double
             lib.orc_e4m3_code.argtypes = [ctypes.c_double]
@@ -253,6 +254,19 @@ def sdpa(q_u16, k_u16, v_u16, rows, *, causal=False):
     rows = _c(rows, np.int64).reshape(-1, 2)
     out = np.empty((rows.shape[0], D))
     lib.orc_sdpa(_p(q), _p(k), _p(v), BH, N, int(causal), _p(rows), rows.shape[0], _p(out))
+    return out
+
+
+def rowsum_parts(P, rule: int = UOS, q: float = 7.25) -> np.ndarray:
+    """Row-sum diagnostic of section 5.5.2 (Fig. 7 B; reading D1 in mxattn_oracle.c):
+    each row of the nonnegative ``P [R, N]`` quantized in 32-key blocks under
+    ``rule``. Returns ``[R, 5]``: sum Q(P), then the zeroing, saturation,
+    downward- and upward-rounding parts of sum(Q(P) - P)."""
+    lib = _load()
+    P = _c(P, np.float64)
+    R, N = P.shape
+    out = np.empty((R, 5))
+    lib.orc_rowsum_parts(_p(P), R, N, int(rule), float(q), _p(out))
     return out
 
 

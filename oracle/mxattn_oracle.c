@@ -48,6 +48,15 @@
  *       Causal: the query's own 16-token V block uses the bf16 V rows (R6).
  *   N6  Q and K are not rotated.
  *
+ * Row-sum diagnostic of a quantized materialized P (section 5.5.2, Fig. 7 B):
+ *   D1  Each row of P is quantized in blocks of 32 consecutive keys counted
+ *       from key 0 (R4), with the block quantizer of Algorithm 1 under the
+ *       given scale rule. The row-sum error sum(Q(P) - P) is split by the
+ *       outcome of each element with P > 0: zeroing (Q(P) = 0), saturation
+ *       (P / 2^e above the largest E2M1 value 6, so Q(P) = 6 * 2^e),
+ *       downward rounding (any other Q(P) < P) and upward rounding
+ *       (Q(P) > P). The four parts sum to the whole error.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared [-fopenmp] -lm
  */
 #include <math.h>
@@ -569,6 +578,40 @@ int orc_forward_nvfp4(const uint8_t* qc, const uint8_t* qs, float q_et, const ui
   free(V);
   free(Vr);
   return 0;
+}
+
+/* ------------------------------------ row-sum diagnostic, section 5.5.2 (D1)
+ * P: R rows of N nonnegative values (row-major). out: R x 5 doubles per row:
+ * sum Q(P), then the zeroing, saturation, downward- and upward-rounding parts
+ * of sum(Q(P) - P). rule / q: scale rule as for the quantizers.              */
+void orc_rowsum_parts(const double* P, int64_t R, int64_t N, int rule, double q, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; r++) {
+    const double* row = P + r * N;
+    double sum = 0.0, zero = 0.0, sat = 0.0, down = 0.0, up = 0.0;
+    for (int64_t k0 = 0; k0 < N; k0 += ORC_BLOCK) {
+      const int n = (int)(N - k0 < ORC_BLOCK ? N - k0 : ORC_BLOCK);
+      double v[ORC_BLOCK];
+      uint8_t c[ORC_BLOCK];
+      for (int i = 0; i < n; i++) v[i] = row[k0 + i];
+      const int sbyte = quantize_block(v, n, rule, q, c);
+      for (int i = 0; i < n; i++) {
+        const double qv = dq(c[i], (uint8_t)sbyte);
+        const double d = qv - v[i];
+        sum += qv;
+        if (v[i] <= 0.0) continue;
+        if (qv == 0.0) zero += d;
+        else if (ldexp(v[i], 127 - sbyte) > 6.0) sat += d;
+        else if (d < 0.0) down += d;
+        else if (d > 0.0) up += d;
+      }
+    }
+    out[5 * r + 0] = sum;
+    out[5 * r + 1] = zero;
+    out[5 * r + 2] = sat;
+    out[5 * r + 3] = down;
+    out[5 * r + 4] = up;
+  }
 }
 
 /* ------------------------------------------- unquantized attention, Eq. 1
