@@ -681,6 +681,59 @@ def run_qmax_sweep(mx, W, names):
     return res
 
 
+def rowsum_parts_gpu(mx, Pb, rule: int):
+    """Section 5.5.2 row-sum diagnostic on the GPU: the bf16 rows ``Pb [R, npad]``
+    (npad a multiple of 128, padding zero) quantized in 32-key blocks by the
+    library's Q/K quantizer (rotation off) under ``rule``. Returns float64
+    ``[R, 5]``: sum Q(P), then the zeroing, saturation (P / 2^e above 6, e the
+    block's scale exponent from the quantizer), downward- and upward-rounding
+    parts of sum(Q(P) - P)."""
+    import torch
+
+    R, npad = Pb.shape
+    rows = R * npad // 128
+    x = Pb.reshape(1, 1, rows, 128)
+    c, sc = mx.mxattn_quantize_qk_ex(x, rule=rule, rotate=False)
+    Qp = _dequant_qk(c, sc, 1, rows).reshape(R, npad).double()
+    Pr = Pb.double()
+    NT = (rows + 127) // 128
+    e = (sc.view(1, NT, 512)[:, :, _atom_rows(sc.device)].reshape(1, NT * 128, 4)[:, :rows].long() - 127)
+    e = e.repeat_interleave(32, -1).reshape(R, npad).double()
+    d = Qp - Pr
+    pos = Pr > 0
+    zero = (Qp == 0) & pos
+    sat = (Pr * torch.exp2(-e) > 6) & pos & ~zero
+    down = (d < 0) & pos & ~zero & ~sat
+    up = (d > 0) & pos
+    return torch.stack([Qp.sum(1)] + [(d * m).sum(1) for m in (zero, sat, down, up)], 1)
+
+
+def materialized_p(W, w, rows_per_workload: int, seed: int = 4321):
+    """Softmax rows P = softmax(QK^T / sqrt(d)) (float64, exact S from the bf16
+    Q and K; causal rows masked) for up to four sampled heads of `w`, and the
+    same rows rounded to bf16 and zero-padded to a multiple of 128 keys."""
+    import torch
+
+    q, k, _ = W.generate(w, device="cuda")
+    B, H, N = w.B, w.H, w.N
+    g = torch.Generator().manual_seed(seed)
+    heads = torch.randperm(B * H, generator=g)[: min(4, B * H)].tolist()
+    per = max(1, rows_per_workload // len(heads))
+    qf, kf = q.reshape(B * H, N, 128), k.reshape(B * H, N, 128)
+    Ps = []
+    for h in heads:
+        ii = torch.randint(0, N, (per,), generator=g).cuda()
+        s = (qf[h, ii].double() @ kf[h].double().T) / 128 ** 0.5
+        if w.causal:
+            s = s.masked_fill(torch.arange(N, device="cuda")[None, :] > ii[:, None], -float("inf"))
+        Ps.append(torch.softmax(s, 1))
+    P = torch.cat(Ps)
+    npad = (N + 127) // 128 * 128
+    Pb = torch.zeros((P.shape[0], npad), dtype=torch.bfloat16, device="cuda")
+    Pb[:, :N] = P.to(torch.bfloat16)
+    return P, Pb
+
+
 def run_rowsum_diagnostic(mx, W, names, rows_per_workload=256):
     """Section 5.5.2 on synthetic heads: materialize P = softmax(S) for sampled rows
     (exact S from the bf16 Q, K), round it to bf16, quantize it in 32-key MXFP4
@@ -692,41 +745,13 @@ def run_rowsum_diagnostic(mx, W, names, rows_per_workload=256):
     out = {}
     for wname in names:
         w = W.WORKLOADS[wname]
-        q, k, _ = W.generate(w, device="cuda")
-        B, H, N = w.B, w.H, w.N
-        g = torch.Generator().manual_seed(4321)
-        heads = torch.randperm(B * H, generator=g)[: min(4, B * H)].tolist()
-        per = max(1, rows_per_workload // len(heads))
-        qf, kf = q.reshape(B * H, N, 128), k.reshape(B * H, N, 128)
-        Ps = []
-        for h in heads:
-            ii = torch.randint(0, N, (per,), generator=g).cuda()
-            s = (qf[h, ii].double() @ kf[h].double().T) / 128 ** 0.5
-            if w.causal:
-                s = s.masked_fill(torch.arange(N, device="cuda")[None, :] > ii[:, None], -float("inf"))
-            Ps.append(torch.softmax(s, 1))
-        P = torch.cat(Ps)                                          # [R, N] float64
+        P, Pb = materialized_p(W, w, rows_per_workload)
         R = P.shape[0]
-        npad = (N + 127) // 128 * 128
-        Pb = torch.zeros((R, npad), dtype=torch.bfloat16, device="cuda")
-        Pb[:, :N] = P.to(torch.bfloat16)
-        Pr = Pb.double()                                           # what the quantizer sees
-        x = Pb.reshape(1, 1, R * npad // 128, 128)
         ent = -(P * torch.log(P.clamp_min(1e-300))).sum(1)
         res = {}
         for rname, rule in (("UOS", 0), ("OCP", 1)):
-            c, sc = mx.mxattn_quantize_qk_ex(x, rule=rule, rotate=False)
-            Qp = _dequant_qk(c, sc, 1, R * npad // 128).reshape(R, npad).double()
-            d = Qp - Pr
-            blk = Pr.reshape(R, npad // 32, 32).amax(2, keepdim=True)
-            e = torch.ceil(torch.log2(blk / 7.25)) if rule == 0 else torch.floor(torch.log2(blk)) - 2
-            sat = (Pr.reshape(R, npad // 32, 32) / torch.exp2(e) > 6).reshape(R, npad) & (Pr > 0)
-            zero = (Qp == 0) & (Pr > 0)
-            down = (d < 0) & ~zero & ~sat
-            up = d > 0
-            rs = Qp.sum(1)
-            parts = {name: (d * m).sum(1).mean().item() for name, m in
-                     (("zeroing", zero), ("saturation", sat), ("rounding_down", down), ("rounding_up", up))}
+            parts = rowsum_parts_gpu(mx, Pb, rule)
+            rs = parts[:, 0]
             bins = {}
             for lo, hi in ((0, 1), (1, 3), (3, 5), (5, 1e9)):
                 m = (ent >= lo) & (ent < hi)
@@ -735,9 +760,12 @@ def run_rowsum_diagnostic(mx, W, names, rows_per_workload=256):
                         "rows": int(m.sum()), "mean_rowsum": rs[m].mean().item(),
                         "frac_below_1": (rs[m] < 1).double().mean().item()}
             res[rname] = {"mean_rowsum": rs.mean().item(), "min_rowsum": rs.min().item(),
-                          "max_rowsum": rs.max().item(), "error_parts": parts, "by_entropy": bins}
+                          "max_rowsum": rs.max().item(),
+                          "error_parts": {name: parts[:, i + 1].mean().item() for i, name in
+                                          enumerate(("zeroing", "saturation", "rounding_down", "rounding_up"))},
+                          "by_entropy": bins}
         out[wname] = {"rows": R, "mean_entropy": ent.mean().item(), "results": res}
-        del q, k
+        del P, Pb
         torch.cuda.empty_cache()
     return out
 

@@ -187,3 +187,21 @@ def test_causal_prefix_mode_no_future_leakage(mx):
                 t[0, 0, i + 1:] = (torch.randn(n, 128, generator=g) * 40).to(t.dtype).to(t.device)
         pert = _run_gpu(mx, q2, k2, v2, 0, True, 0, 2)
         assert np.array_equal(pert[0, i], base[0, i]), f"row {i} changed"
+
+
+@pytest.mark.parametrize("name", ["causal_lm_8192", "wan_32760"])
+def test_rowsum_diagnostic_matches_oracle(mx, orc, name):
+    """bench.py --accuracy's row-sum diagnostic (section 5.5.2, Fig. 7 B), computed
+    on the GPU through the library's quantizer, against the oracle's
+    rowsum_parts on the same bf16 rows: row sum and the zeroing / saturation /
+    downward / upward rounding parts, per row, under UOS and the OCP rule."""
+    import bench
+    from mxfp4_precision_attention_gb300 import workloads as W
+
+    P, Pb = bench.materialized_p(W, W.WORKLOADS[name], 24)
+    Pr = Pb.double().cpu().numpy()
+    for rule in (orc.UOS, orc.OCP):
+        g = bench.rowsum_parts_gpu(mx, Pb, rule).cpu().numpy()
+        ref = orc.rowsum_parts(Pr, rule)
+        assert np.allclose(g, ref, rtol=1e-12, atol=1e-12), np.abs(g - ref).max()
+        assert np.allclose(g[:, 0] - Pr.sum(1), g[:, 1:].sum(1), rtol=0, atol=1e-12)
