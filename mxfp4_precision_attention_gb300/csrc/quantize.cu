@@ -545,6 +545,114 @@ __global__ void __launch_bounds__(kQThreads, kQMinBlocks)
   }
 }
 
+// ----------------------------------------------------- fused Q/K/V by role
+// The one-launch quantizer of a forward (mxattn_quantize_qkv: Q and K rotated,
+// V not, MXFP4) with the work split by role inside one CTA per SM: warpgroups
+// 0 and 1 take the Q and K tiles (one thread per token, 200 registers), and
+// warpgroup 2 the V tiles (104 registers; setmaxnreg moves the difference:
+// 2 * 128 * 200 + 128 * 104 = 384 * 168, the launch allocation).
+// Each warpgroup has its own two-stage TMA ring and leader thread. Three warps
+// then share every SM sub-partition, and the V tiles' light, memory-bound
+// work runs beside the rotation's ALU work instead of taking turns with it.
+// Same per-tile code (quantize_qk_tile, quantize_v_tile), so the same bytes.
+constexpr int kRThreads = 384;
+constexpr int kRStages = 2;
+constexpr uint32_t kRRingBytes = kRStages * kQStageBytes;                // 64 KB per warpgroup
+constexpr uint32_t kRSmemBytes = 3 * kRRingBytes + 3 * 2 * kRStages * 8 + 16 + 1024;
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    quantize_qkv_roles_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+                              const __grid_constant__ CUtensorMap m2, const __grid_constant__ QParams p) {
+  extern __shared__ __align__(1024) uint8_t qsmem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 3 * kRRingBytes);  // [3 rings][full, empty][stages]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * 2 * kRStages);
+  const int wg = threadIdx.x / 128;     // 0, 1: Q/K tiles; 2: V tiles
+  const int t128 = threadIdx.x % 128;   // thread within the warpgroup
+  const int wwarp = t128 / 32, lane = t128 % 32;
+  const bool leader = t128 == 0;
+  const uint32_t ring = smem_u32(smem + wg * kRRingBytes);
+  auto full = [&](int s) { return smem_u32(&bars[(wg * 2 + 0) * kRStages + s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[(wg * 2 + 1) * kRStages + s]); };
+  const int64_t G = gridDim.x, c = blockIdx.x;
+  const int64_t U = p.BH * p.NT;  // tiles per tensor
+  // this warpgroup's units: Q/K unit u (tensor u % 2, tile u / 2) for u = c + i*G,
+  // i = wg, wg + 2, ...; V tile c + i*G for i = 0, 1, ...
+  const int64_t first = wg < 2 ? c + wg * G : c;
+  const int64_t step = wg < 2 ? 2 * G : G;
+  const int64_t total = wg < 2 ? 2 * U : U;
+  const uint32_t nunits = first < total ? static_cast<uint32_t>((total - first + step - 1) / step) : 0u;
+  auto issue = [&](uint32_t j) {
+    const int64_t u = first + static_cast<int64_t>(j) * step;
+    const int ti = wg < 2 ? static_cast<int>(u % 2) : 2;
+    const int64_t tile = wg < 2 ? u / 2 : u;
+    const int bh = static_cast<int>(tile / p.NT);
+    const int t = static_cast<int>(tile - static_cast<int64_t>(bh) * p.NT);
+    const CUtensorMap* m = ti == 0 ? &m0 : (ti == 1 ? &m1 : &m2);
+    const int s = j % kRStages;
+    mbar_arrive_expect_tx(full(s), kQStageBytes);
+    tma_load_3d(ring + s * kQStageBytes, m, full(s), 0, t * kTile, bh);
+    tma_load_3d(ring + s * kQStageBytes + kQHalfBytes, m, full(s), 64, t * kTile, bh);
+  };
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int r = 0; r < 3; r++)
+      for (int s = 0; s < kRStages; s++) {
+        mbar_init(smem_u32(&bars[(r * 2 + 0) * kRStages + s]), 1);
+        mbar_init(smem_u32(&bars[(r * 2 + 1) * kRStages + s]), 4);
+      }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // One warpgroup's loop: the leader keeps kRStages units in flight; unit i-1's
+  // stage is refilled with unit i-1+kRStages once the warpgroup's four warps
+  // have read unit i-1 into registers.
+  auto run = [&](auto&& quantize_unit) {
+    uint32_t issued = 0;
+    if (leader) {
+      prefetch_tmap(wg == 2 ? &m2 : (wg == 0 ? &m0 : &m1));
+      for (; issued < nunits && issued < static_cast<uint32_t>(kRStages); issued++) issue(issued);
+    }
+    for (uint32_t i = 0; i < nunits; i++) {
+      if (leader && i >= 1 && issued < nunits) {
+        const uint32_t prev = i - 1;
+        if (!mbar_wait(empty(prev % kRStages), (prev / kRStages) & 1, abort_flag)) {
+          record_error(p.status, 4, const_cast<int*>(abort_flag));
+        } else {
+          issue(issued);
+          issued++;
+        }
+      }
+      const int s = i % kRStages;
+      if (!mbar_wait(full(s), (i / kRStages) & 1, abort_flag)) {
+        record_error(p.status, 4, const_cast<int*>(abort_flag));
+        break;
+      }
+      quantize_unit(first + static_cast<int64_t>(i) * step, smem + wg * kRRingBytes + s * kQStageBytes, empty(s));
+    }
+    // after an abort, every copy the leader issued must land before the CTA exits
+    if (leader && *abort_flag) {
+      for (uint32_t j = 0; j < issued; j++) mbar_wait(full(j % kRStages), (j / kRStages) & 1, abort_flag);
+    }
+  };
+  // each role's code sits wholly inside its own branch, after its register change
+  if (wg < 2) {
+    regs_inc<200>();
+    run([&](int64_t u, const uint8_t* st, uint32_t eb) {
+      const int64_t tile = u / 2;
+      const int64_t bh = tile / p.NT;
+      const QTensor T = (u % 2) == 0 ? p.t[0] : p.t[1];
+      quantize_qk_tile(st, t128, bh, tile - bh * p.NT, p, T, eb);
+    });
+  } else {
+    regs_dec<104>();
+    run([&](int64_t u, const uint8_t* st, uint32_t eb) {
+      const int64_t bh = u / p.NT;
+      quantize_v_tile(st, wwarp, lane, bh, u - bh * p.NT, p, p.t[2], eb);
+    });
+  }
+}
+
 }  // namespace
 
 void rule_threshold(int rule, double qmax, uint32_t* mant_thr, uint32_t* pow2_down) {
@@ -594,7 +702,16 @@ cudaError_t launch_quantize(const QuantizeJob* jobs, int njobs, int64_t BH, int6
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(quantize_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(quantize_qkv_roles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+    if (e != cudaSuccess) return e;
     attr_set[dev] = true;
+  }
+  // the forward's one-launch quantizer (rotated Q and K, then V, MXFP4): the role-split kernel
+  if (njobs == 3 && !p.t[0].nv && !p.t[1].nv && !p.t[2].nv && !p.t[0].is_v && !p.t[1].is_v && p.t[2].is_v) {
+    const int64_t U = BH * NT;
+    const int grid = static_cast<int>(U < sms[dev] ? U : sms[dev]);
+    quantize_qkv_roles_kernel<<<grid, kRThreads, kRSmemBytes, s>>>(maps[0], maps[1], maps[2], p);
+    return cudaGetLastError();
   }
   // NVFP4 jobs: the tensor maximum first (the encode factor needs it)
   for (int j = 0; j < njobs; j++) {
