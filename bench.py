@@ -570,7 +570,7 @@ def run_ours(args, w):
                          "peak_source": f"{peak_src} bf16 {bf16:.1f} TF/s x nominal fp4/bf16 ratio {FP4_OVER_BF16_NOMINAL:g}"},
             "breakdown_ms": {"quantize_qkv": qkv_ms, "forward": fwd_ms},
             "forward_out_bf16_ms": fwd_bf16out_ms,
-            "quantizer": {"kernel": "quantize_tiles_kernel (one launch for Q, K, V)",
+            "quantizer": {"kernel": "quantize_qkv_roles_kernel (one launch for Q, K, V)",
                           "algorithmic_bytes": qkv_bytes, "gbs": qkv_bytes / (qkv_ms * 1e-3) / 1e9,
                           "frac_of_hbm": qkv_bytes / (qkv_ms * 1e-3) / 1e9 / hbm, "hbm_peak": hbm,
                           "single_calls": single},
