@@ -206,6 +206,28 @@ __device__ __forceinline__ float e2m1_decode(uint32_t nib) {
   return (nib & 8u) ? -mag : mag;
 }
 
+// Four non-negative E2M1 codes (the nibbles of the low 16 bits of c) as two
+// bf16x2 words, elements (0, 1) and (2, 3). A non-negative code is a byte
+// index 0-7, so one byte permute looks up the high bytes of all four bf16
+// values {0, 0.5, 1, 1.5, 2, 3, 4, 6} and one the low bytes.
+__device__ __forceinline__ void e2m1x4_bf16(uint32_t c, uint32_t& w01, uint32_t& w23) {
+  const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, c);
+  const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, c);
+  w01 = __byte_perm(lo, hi, 0x5140u);
+  w23 = __byte_perm(lo, hi, 0x7362u);
+}
+// The eight non-negative E2M1 codes of w (element k in nibble k) as binary32.
+__device__ __forceinline__ void e2m1x8_f32(uint32_t w, float (&x)[8]) {
+  uint32_t b[4];
+  e2m1x4_bf16(w & 0xFFFFu, b[0], b[1]);
+  e2m1x4_bf16(w >> 16, b[2], b[3]);
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    x[2 * i] = __uint_as_float(b[i] << 16);
+    x[2 * i + 1] = __uint_as_float(b[i] & 0xFFFF0000u);
+  }
+}
+
 // Block exponent of a finite maximum M > 0 under a scale rule given by its
 // mantissa threshold (the quantizers' rule); denormal maxima clamp to -127.
 __device__ __forceinline__ int rule_exponent(float M, uint32_t mant_thr, uint32_t pow2_down) {
@@ -791,6 +813,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (Tg > 0) {
       wait_uniform(kBarODone + g, (Tg - 1) & 1);
       tc_fence_after();
+      // Causal: the diagonal tile's bf16 V rows for the product below, loaded
+      // first so that the load overlaps the rest of the epilogue. Group A uses
+      // its own 64 KB region. Group B puts its V in the K ring: B's last P^V^
+      // is complete, and every QK^T that read the ring completed before it.
+      [[maybe_unused]] const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
+      [[maybe_unused]] const bool dleader = quad == 0 && lane == 0;
+      if constexpr (kDiagMma) {
+        if (!(kVariant && p.causal == 2) && dleader && !my_abort) {
+          mbar_arrive_expect_tx(bar(kBarDiagV + g), 32768);
+          tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV + g), 0, (Tg - 1) * kTile, bh);
+          tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV + g), 64, (Tg - 1) * kTile, bh);
+        }
+      }
       if (!my_abort) {
         uint32_t lbits = tmem_ld1(tl + ocol + kD);
         tmem_wait_ld();
@@ -804,7 +839,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // placement already counted its P~
           if (!direct) {
 #pragma unroll
-            for (int k = 0; k < 32; k++) l += e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
+            for (int kk = 0; kk < 4; kk++) {
+              float x[8];
+              e2m1x8_f32(diag_words[kk], x);
+#pragma unroll
+              for (int k = 0; k < 8; k++) l += x[k] * dsc;
+            }
           }
         }
         if (direct) l = l_direct;
@@ -913,19 +953,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The diagonal block's product on the tensor cores: this row's P^ on its
           // own 32-key block (zero beyond the row and outside the block; exact in
           // bf16, an E2M1 value times a power of two) times the diagonal tile's
-          // bf16 V rows, one kind::f16 128x128x128 product accumulated into O_g
-          // after its last P^V^; every wait is bounded. Group A uses its own
-          // 64 KB region. Group B's operands go to the K ring (its V) and the V
-          // ring (its P^): B's epilogue starts once its last P^V^ is complete, and
-          // every QK^T and P^V^ that read the rings completed before that one.
-          const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
+          // bf16 V rows (loaded at the start of the epilogue), one kind::f16
+          // 128x128x128 product accumulated into O_g after its last P^V^; every
+          // wait is bounded. Group A uses its own 64 KB region. Group B's P^ goes
+          // to the V ring: every P^V^ that read it completed before B's last one.
           uint8_t* pdiag = g ? smem + kOffV : smem + kOffDiag + 32768;  // [keys 0-63 | 64-127][128 rows][128 B]
-          const bool leader = quad == 0 && lane == 0;
-          if (leader && !my_abort) {
-            mbar_arrive_expect_tx(bar(kBarDiagV + g), 32768);
-            tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV + g), 0, (Tg - 1) * kTile, bh);
-            tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV + g), 64, (Tg - 1) * kTile, bh);
-          }
+          const bool leader = dleader;
           if constexpr (kNv) {
             // O_g holds V^'s encoded units (x e_tV): bring this row to real units
             // first, so the product with the real bf16 V adds in place and the
@@ -950,11 +983,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           {
             uint32_t pw[16];  // this row's P^ on keys 32*quad .. +31 as bf16 pairs
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float a0 = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8))) & 0xFu) * dsc;
-              const float a1 = e2m1_decode((diag_words[k / 8] >> (4 * (k % 8 + 1))) & 0xFu) * dsc;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-              pw[k / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int kk = 0; kk < 4; kk++) {
+              float x[8];
+              e2m1x8_f32(diag_words[kk], x);
+#pragma unroll
+              for (int k = 0; k < 8; k += 2) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[k] * dsc, x[k + 1] * dsc);
+                pw[4 * kk + k / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
             }
             const int x = r & 7, own_half = quad >> 1, own_c0 = 4 * (quad & 1);
 #pragma unroll
