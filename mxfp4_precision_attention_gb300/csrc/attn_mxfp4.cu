@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t diag_sbyte = 127;
     float diag_s = 0.0f;  // NVFP4: E4M3 scale value of the query's own 16-key block
     float l_direct = 0.0f;  // variant kernels, direct placement: l from P~ (Eq. 16)
+    bool dv_pending = false;  // causal: this thread's diagonal V load not yet seen to land
     // all lanes poll; the outcome is made warp-uniform so tcgen05 .sync.aligned ops stay convergent
     auto wait_uniform = [&](int b, uint32_t parity) {
       bool ok = !my_abort && mbar_wait(bar(b), parity, abort_flag);
@@ -560,6 +561,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const bool masked = j == Tg - 1 && (kCausal || ragged);
       if (masked) {
+        if constexpr (kDiagMma) {
+          // Causal, the group's last (diagonal) key tile: its bf16 V rows for the
+          // epilogue's diagonal product start loading now. Group A uses its own
+          // 64 KB region. Group B puts them in the K ring: the S just read came
+          // from the CTA's last QK^T, so every product that read the ring is
+          // complete, and so is every load into it.
+          if (!(kVariant && p.causal == 2) && quad == 0 && lane == 0) {
+            const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
+            mbar_arrive_expect_tx(bar(kBarDiagV + g), 32768);
+            tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV + g), 0, j * kTile, bh);
+            tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV + g), 64, j * kTile, bh);
+            dv_pending = true;
+          }
+        }
         // keys of this tile visible to the row: i < nvalid (key < N, and key <= row if causal)
         const int64_t key0 = static_cast<int64_t>(j) * kTile;
         int64_t lim = N - key0;
@@ -813,19 +828,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (Tg > 0) {
       wait_uniform(kBarODone + g, (Tg - 1) & 1);
       tc_fence_after();
-      // Causal: the diagonal tile's bf16 V rows for the product below, loaded
-      // first so that the load overlaps the rest of the epilogue. Group A uses
-      // its own 64 KB region. Group B puts its V in the K ring: B's last P^V^
-      // is complete, and every QK^T that read the ring completed before it.
-      [[maybe_unused]] const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
-      [[maybe_unused]] const bool dleader = quad == 0 && lane == 0;
-      if constexpr (kDiagMma) {
-        if (!(kVariant && p.causal == 2) && dleader && !my_abort) {
-          mbar_arrive_expect_tx(bar(kBarDiagV + g), 32768);
-          tma_load_3d(vdiag, &tm_vb, bar(kBarDiagV + g), 0, (Tg - 1) * kTile, bh);
-          tma_load_3d(vdiag + 16384, &tm_vb, bar(kBarDiagV + g), 64, (Tg - 1) * kTile, bh);
-        }
-      }
       if (!my_abort) {
         uint32_t lbits = tmem_ld1(tl + ocol + kD);
         tmem_wait_ld();
@@ -953,12 +955,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The diagonal block's product on the tensor cores: this row's P^ on its
           // own 32-key block (zero beyond the row and outside the block; exact in
           // bf16, an E2M1 value times a power of two) times the diagonal tile's
-          // bf16 V rows (loaded at the start of the epilogue), one kind::f16
+          // bf16 V rows (loaded since the group read its last S), one kind::f16
           // 128x128x128 product accumulated into O_g after its last P^V^; every
           // wait is bounded. Group A uses its own 64 KB region. Group B's P^ goes
           // to the V ring: every P^V^ that read it completed before B's last one.
+          const uint32_t vdiag = g ? sb + kOffK : sb + kOffDiag;  // [channels 0-63 | 64-127][128 keys][128 B]
           uint8_t* pdiag = g ? smem + kOffV : smem + kOffDiag + 32768;  // [keys 0-63 | 64-127][128 rows][128 B]
-          const bool leader = dleader;
+          const bool leader = quad == 0 && lane == 0;
           if constexpr (kNv) {
             // O_g holds V^'s encoded units (x e_tV): bring this row to real units
             // first, so the product with the real bf16 V adds in place and the
@@ -1015,6 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             bool ok = !my_abort && mbar_wait(bar(kBarDiagP + g), 0, abort_flag) &&
                       mbar_wait(bar(kBarDiagV + g), 0, abort_flag);
+            dv_pending = dv_pending && !ok;
             if (ok) {
               tc_fence_after();
               const uint32_t idd = idesc_bf16(128, 128, true);
@@ -1163,6 +1167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // after an abort, a diagonal V load issued in the last key tile must land
+    // before the CTA exits (bounded, like every wait)
+    if (dv_pending) mbar_wait(bar(kBarDiagV + g), 0, abort_flag);
   }
 
   tc_fence_before();
