@@ -27,9 +27,11 @@
 //
 // Causal mode (MatX note "leaky quantization"): keys j > i are masked before
 // the maximum, tiles past the diagonal are skipped, and for the 32-token V
-// block holding the query, P^ multiplies the bf16 V rows instead of V^ (formed
-// on CUDA cores in the epilogue from the codes the thread kept; the block's
-// codes are zeroed in the tensor-core operand and its sum is added to l).
+// block holding the query, P^ multiplies the bf16 V rows instead of V^: the
+// block's codes are zeroed in the P^V^ operand, kept by the thread, added to
+// l, and multiplied with the diagonal tile's bf16 V rows in the epilogue by
+// one kind::f16 tensor-core product into O (causal mode 2, the re-quantized
+// diagonal block, does that product on CUDA cores instead).
 //
 // Every mbarrier wait is bounded (~1 s); on expiry the kernel records an error
 // in the device status word, the waiting warp leaves its loop, and TMEM is
