@@ -93,8 +93,8 @@ MXATTN_API mxattn_status mxattn_quantize_v(const void* v, int64_t B, int64_t H, 
  * and the block quantization act on Q/K tiles locally, so they belong in the
  * Q/K preprocessing stage). Writes exactly what mxattn_rotate_quantize_qk(q),
  * mxattn_rotate_quantize_qk(k) and mxattn_quantize_v(v) write, byte for byte,
- * from one persistent kernel in which the 128-token tiles of the three
- * tensors interleave.
+ * from one kernel with one CTA per SM, in which two warpgroups take the Q and
+ * K tiles and a third the V tiles (128 tokens of one head per tile).
  *   q, k, v                            : bf16 [B, H, N, 128] (device, read only)
  *   q_codes/q_scales, k_codes/k_scales : as for mxattn_rotate_quantize_qk
  *   v_codes/v_scales                   : as for mxattn_quantize_v

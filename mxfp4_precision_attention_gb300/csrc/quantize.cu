@@ -2,8 +2,10 @@
 // and quantization steps of Algorithm 2 in section 4.3, with the UOS block
 // quantizer of Algorithm 1).
 //
-// Both run in one kernel (quantize_tiles_kernel below), one launch per call;
-// mxattn_quantize_qkv runs all three tensors of a forward in one launch.
+// One launch per call. The single-tensor calls, the ablation rules and NVFP4
+// run quantize_tiles_kernel; mxattn_quantize_qkv (the forward's Q, K and V,
+// MXFP4) runs quantize_qkv_roles_kernel, the same per-tile code with the
+// work split by role among three warpgroups.
 //
 //  (a) rotate_quantize_qk: per token, Hadamard-rotate the 128 channels
 //      (binary32 butterflies h = 1,2,...,64, then x 2^-3.5 rounded to binary32)
