@@ -538,17 +538,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_uniform(kBarSFull + g, j & 1);
       if (my_abort) break;
       tc_fence_after();
+      float bm_ld[4];  // MXFP4: the 32-key block maxima of the row, from the loads themselves
       {
         uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tl + kColS, r0);
-        tmem_ld32(tl + kColS + 32, r1);
-        tmem_ld32(tl + kColS + 64, r2);
-        tmem_ld32(tl + kColS + 96, r3);
+        if constexpr (kNv) {
+          tmem_ld32(tl + kColS, r0);
+          tmem_ld32(tl + kColS + 32, r1);
+          tmem_ld32(tl + kColS + 64, r2);
+          tmem_ld32(tl + kColS + 96, r3);
+        } else {
+          tmem_ld32_max(tl + kColS, r0, bm_ld[0]);
+          tmem_ld32_max(tl + kColS + 32, r1, bm_ld[1]);
+          tmem_ld32_max(tl + kColS + 64, r2, bm_ld[2]);
+          tmem_ld32_max(tl + kColS + 96, r3, bm_ld[3]);
+        }
         tmem_wait_ld();
         reg_fence32(r0);
         reg_fence32(r1);
         reg_fence32(r2);
         reg_fence32(r3);
+        if constexpr (!kNv) {
+#pragma unroll
+          for (int b = 0; b < 4; b++) {
+            uint32_t u = __float_as_uint(bm_ld[b]);
+            reg_fence1(u);
+            bm_ld[b] = __uint_as_float(u);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           v[i] = __uint_as_float(r0[i]);
@@ -673,9 +689,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tmem_wait_st();
       } else {
+        // the last tile's masked keys are -inf in v only: its maxima come from v
         float bm[4];
 #pragma unroll
-        for (int b = 0; b < 4; b++) bm[b] = max32(v + 32 * b);
+        for (int b = 0; b < 4; b++) bm[b] = masked ? max32(v + 32 * b) : bm_ld[b];
         m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
         const float mc = m_new * C;
 
