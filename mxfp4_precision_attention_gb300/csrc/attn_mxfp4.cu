@@ -538,32 +538,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_uniform(kBarSFull + g, j & 1);
       if (my_abort) break;
       tc_fence_after();
-      float bm_ld[4];  // MXFP4: the 32-key block maxima of the row, from the loads themselves
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        if constexpr (kNv) {
-          tmem_ld32(tl + kColS, r0);
-          tmem_ld32(tl + kColS + 32, r1);
-          tmem_ld32(tl + kColS + 64, r2);
-          tmem_ld32(tl + kColS + 96, r3);
-        } else {
-          tmem_ld32_max(tl + kColS, r0, bm_ld[0]);
-          tmem_ld32_max(tl + kColS + 32, r1, bm_ld[1]);
-          tmem_ld32_max(tl + kColS + 64, r2, bm_ld[2]);
-          tmem_ld32_max(tl + kColS + 96, r3, bm_ld[3]);
+      // the row's block maxima (32 keys; NVFP4: 16) from the loads themselves
+      float bm_ld[kNv ? 8 : 4];
+      if constexpr (kNv) {
+        uint32_t r[8][16];
+#pragma unroll
+        for (int b = 0; b < 8; b++) tmem_ld16_max(tl + kColS + 16 * b, r[b], bm_ld[b]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
+          uint32_t u = __float_as_uint(bm_ld[b]);
+          reg_fence1(u);
+          bm_ld[b] = __uint_as_float(u);
+#pragma unroll
+          for (int i = 0; i < 16; i++) {
+            reg_fence1(r[b][i]);
+            v[16 * b + i] = __uint_as_float(r[b][i]);
+          }
         }
+      } else {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32_max(tl + kColS, r0, bm_ld[0]);
+        tmem_ld32_max(tl + kColS + 32, r1, bm_ld[1]);
+        tmem_ld32_max(tl + kColS + 64, r2, bm_ld[2]);
+        tmem_ld32_max(tl + kColS + 96, r3, bm_ld[3]);
         tmem_wait_ld();
         reg_fence32(r0);
         reg_fence32(r1);
         reg_fence32(r2);
         reg_fence32(r3);
-        if constexpr (!kNv) {
 #pragma unroll
-          for (int b = 0; b < 4; b++) {
-            uint32_t u = __float_as_uint(bm_ld[b]);
-            reg_fence1(u);
-            bm_ld[b] = __uint_as_float(u);
-          }
+        for (int b = 0; b < 4; b++) {
+          uint32_t u = __float_as_uint(bm_ld[b]);
+          reg_fence1(u);
+          bm_ld[b] = __uint_as_float(u);
         }
 #pragma unroll
         for (int i = 0; i < 32; i++) {
@@ -611,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P~ / S and its E2M1 code is the block's code.
         float bm[8];
 #pragma unroll
-        for (int b = 0; b < 8; b++) bm[b] = max16(v + 16 * b);
+        for (int b = 0; b < 8; b++) bm[b] = masked ? max16(v + 16 * b) : bm_ld[b];
         m_new = fmax3(fmax3(m_run, bm[0], bm[1]), fmax3(bm[2], bm[3], bm[4]), fmax3(bm[5], bm[6], bm[7]));
         const float mc = m_new * C;
         uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
