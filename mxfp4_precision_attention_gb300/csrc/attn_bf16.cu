@@ -236,13 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < T; j++) {
       const int s = j & 1;
       float v[64];
+      float pm = 0.0f;  // this warp's half-row maximum (from the loads themselves)
       wait_uniform(kBarSFull + s, (j >> 1) & 1);
       tc_fence_after();
       if (!my_abort) {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tl + kColS + s * 128 + 64 * h, r0);
-        tmem_ld32(tl + kColS + s * 128 + 64 * h + 32, r1);
+        float m0, m1;
+        tmem_ld32_max(tl + kColS + s * 128 + 64 * h, r0, m0);
+        tmem_ld32_max(tl + kColS + s * 128 + 64 * h + 32, r1, m1);
         tmem_wait_ld();
+        reg_fence32(r0);
+        reg_fence32(r1);
+        uint32_t u0 = __float_as_uint(m0), u1 = __float_as_uint(m1);
+        reg_fence1(u0);
+        reg_fence1(u1);
+        pm = fmaxf(__uint_as_float(u0), __uint_as_float(u1));
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           v[i] = __uint_as_float(r0[i]);
@@ -257,16 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + s));
       const int64_t key0 = static_cast<int64_t>(j) * 128 + 64 * h;
       if (j == T - 1 && (p.causal || ragged)) {
+        // the last tile's masked keys are -inf in v only: its maximum comes from v
 #pragma unroll
         for (int i = 0; i < 64; i++) {
           const int64_t key = key0 + i;
           if (!(key < Nk && (!p.causal || key <= qrow))) v[i] = -INFINITY;
         }
-      }
-      float pm = v[0];
+        pm = v[0];
 #pragma unroll
-      for (int i = 1; i < 63; i += 2) pm = fmax3(pm, v[i], v[i + 1]);
-      pm = fmaxf(pm, v[63]);
+        for (int i = 1; i < 63; i += 2) pm = fmax3(pm, v[i], v[i + 1]);
+        pm = fmaxf(pm, v[63]);
+      }
       xchg[(s * 2 + h) * 128 + r] = pm;
       aborted = bar_red_or(1, 256, my_abort || *abort_flag);
       if (aborted) break;
