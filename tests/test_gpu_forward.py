@@ -235,6 +235,25 @@ def test_bf16_forward_vs_exact_softmax(mx, orc, shape, causal):
     assert err <= 2 * 2 ** -9 * vmax + 1e-5
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_full_length(mx, orc, causal):
+    """BF16 path over a full Wan-length key loop (one head, N = 32760: 256 key
+    tiles, the ragged last one 120 keys long) with the outlier recipe, on
+    sampled rows against fp64 softmax attention. Same bound as above."""
+    N = 32760
+    q, k, v = W.generate(W.WORKLOADS["wan_32760"], device="cuda", B=1, H=1, N=N)
+    out = mx.mxattn_forward_bf16(q, k, v, causal=causal)
+    mx.mxattn_check()
+    rng = np.random.default_rng(5)
+    rows = np.array([[0, int(i)] for i in np.concatenate([rng.integers(0, N, 40), [0, 127, 128, N - 121, N - 1]])])
+    ref = orc.sdpa(W.as_u16(q).reshape(1, N, 128), W.as_u16(k).reshape(1, N, 128), W.as_u16(v).reshape(1, N, 128),
+                   rows, causal=causal)
+    g = out.reshape(1, N, 128)[0, torch.as_tensor(rows[:, 1], device=out.device)].cpu().numpy().astype(np.float64)
+    vmax = float(torch.max(torch.abs(v.float())).item())
+    err = np.abs(g - ref).max()
+    assert err <= 2 * 2 ** -9 * vmax + 1e-5, (err, 2 * 2 ** -9 * vmax)
+
+
 def test_mxfp4_error_vs_unquantized_reported(mx, orc):
     """Error of the MXFP4 path against fp64 unquantized attention: reported, not gated."""
     q, k, v = W.generate(W.WORKLOADS["tiny_outlier_512"], device="cuda")
