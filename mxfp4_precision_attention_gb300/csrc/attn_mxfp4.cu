@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
@@ -755,6 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < 4; b++)
             if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
         }
+        // the code loop, compiled twice in the causal kernels: the diagonal tile's
+        // copy keeps the query's own block aside, the other tiles' copy carries
+        // no trace of it
+        auto code_loop = [&](auto diag_c) {
+          constexpr bool kDiagTile = decltype(diag_c)::value;
 #pragma unroll
         for (int b = 0; b < 4; b++) {
           const float noff = b == 0 ? no01.x : (b == 1 ? no01.y : (b == 2 ? no23.x : no23.y));
@@ -780,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_ptilde = fmaf(ysum.x + ysum.y, scale, tile_ptilde);
           }
           if (kDump && dump != nullptr) *reinterpret_cast<uint4*>(dump + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
-          if (diag_tile && b == quad) {
+          if (kDiagTile && b == quad) {
             // the query's own 32-key block: keep its codes for the bf16-V product,
             // drop it from the tensor-core operand
 #pragma unroll
@@ -792,6 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        };
+        if (kCausal && diag_tile)
+          code_loop(std::true_type{});
+        else
+          code_loop(std::false_type{});
         if (kDump && dump != nullptr)
           *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
         // P^ scales: lane r, column base + r/32 of this group's scale buffer
