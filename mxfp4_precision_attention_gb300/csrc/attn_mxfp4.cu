@@ -609,6 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nvalid = lim < 0 ? 0 : (lim > kTile ? kTile : static_cast<int>(lim));
 #pragma unroll
         for (int i = 0; i < 128; i++) v[i] = (i < nvalid) ? v[i] : -INFINITY;
+        // the masked keys are -inf in v only: this tile's block maxima come from v
+        if constexpr (kNv) {
+#pragma unroll
+          for (int b = 0; b < 8; b++) bm_ld[b] = max16(v + 16 * b);
+        } else {
+#pragma unroll
+          for (int b = 0; b < 4; b++) bm_ld[b] = max32(v + 32 * b);
+        }
       }
       float m_new;
       float tile_ptilde = 0.0f;  // direct placement: sum of this row's P~ over the tile
@@ -620,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P~ / S and its E2M1 code is the block's code.
         float bm[8];
 #pragma unroll
-        for (int b = 0; b < 8; b++) bm[b] = masked ? max16(v + 16 * b) : bm_ld[b];
+        for (int b = 0; b < 8; b++) bm[b] = bm_ld[b];
         m_new = fmax3(fmax3(m_run, bm[0], bm[1]), fmax3(bm[2], bm[3], bm[4]), fmax3(bm[5], bm[6], bm[7]));
         const float mc = m_new * C;
         uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
@@ -698,10 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tmem_wait_st();
       } else {
-        // the last tile's masked keys are -inf in v only: its maxima come from v
         float bm[4];
 #pragma unroll
-        for (int b = 0; b < 4; b++) bm[b] = masked ? max32(v + 32 * b) : bm_ld[b];
+        for (int b = 0; b < 4; b++) bm[b] = bm_ld[b];
         m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
         const float mc = m_new * C;
 
