@@ -587,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kBarSEmpty));
 
       const bool masked = j == Tg - 1 && (kCausal || ragged);
+      uint32_t zmask = 0u;  // MXFP4, non-causal: 0xFF in the byte of each fully masked 32-key block
       if (masked) {
         if constexpr (kDiagMma) {
           // Causal, the group's last (diagonal) key tile: its bf16 V rows for the
@@ -615,7 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < 8; b++) bm_ld[b] = max16(v + 16 * b);
         } else {
 #pragma unroll
-          for (int b = 0; b < 4; b++) bm_ld[b] = max32(v + 32 * b);
+          for (int b = 0; b < 4; b++) {
+            bm_ld[b] = max32(v + 32 * b);
+            if (!kCausal && bm_ld[b] == -INFINITY) zmask |= 0xFFu << (8 * b);
+          }
         }
       }
       float m_new;
@@ -757,11 +761,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 no23 = __fadd2_rn(__ffma2_rn(t23, neg1, mg), nmc);
         uint32_t sbytes = __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
                                       __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
-        if (masked) {
-          // all-zero (fully masked) blocks take sigma = 1
+        // all-zero (fully masked) blocks take sigma = 1. Without causality the
+        // blocks were marked where the last tile was masked (a branch here was
+        // executed as predicated code in every tile); the causal kernels keep
+        // the branch, which times faster there.
+        if constexpr (kCausal) {
+          if (masked) {
 #pragma unroll
-          for (int b = 0; b < 4; b++)
-            if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
+            for (int b = 0; b < 4; b++)
+              if (bm[b] == -INFINITY) sbytes = (sbytes & ~(0xFFu << (8 * b))) | (127u << (8 * b));
+          }
+        } else {
+          sbytes = (sbytes & ~zmask) | (0x7F7F7F7Fu & zmask);
         }
         // the code loop, compiled twice in the causal kernels: the diagonal tile's
         // copy keeps the query's own block aside, the other tiles' copy carries
@@ -813,9 +824,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kDump && dump != nullptr)
           *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
         // P^ scales: lane r, column base + r/32 of this group's scale buffer
+        // (the store is waited for with the O rescale's, before p_full)
         tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
         fence_proxy_async_smem();
-        tmem_wait_st();
       }
       if constexpr (kVariant) l_direct = fmaf(ex2_approx((m_run - m_new) * C), l_direct, tile_ptilde);
       if (j >= 1) {
@@ -860,9 +871,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tl + ocol + 64, o2);
           tmem_st32(tl + ocol + 96, o3);
           tmem_st1(tl + ocol + kD, __float_as_uint(__uint_as_float(l) * alpha));
-          tmem_wait_st();
         }
       }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull + g));
