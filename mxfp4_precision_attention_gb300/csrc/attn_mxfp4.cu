@@ -5,7 +5,7 @@
 //   S_j   = Q^ K^_j^T                 tcgen05.mma kind::mxf4 block_scale -> TMEM
 //   m_j   = max(m_{j-1}, rowmax S_j / sqrt(d))
 //   P~    = exp(S_j / sqrt(d) - m_j)             (registers only)
-//   P^    = Q*(P~) per 32-key block, UOS scale   (codes -> smem, scales -> TMEM)
+//   P^    = Q*(P~) per 32-key block, UOS scale   (codes and scales -> TMEM)
 //   O     = diag(alpha) O + P^ [V^ | 1]          tcgen05.mma kind::mxf4 -> TMEM
 // V^ is extended with 16 rows of ones, so the same MMA that accumulates P^ V^
 // also accumulates l = sum P^ in column 128 of the O tile: the row sum and the
@@ -20,10 +20,12 @@
 //   4-7   softmax of tile A, 8-11 softmax of tile B: one full query row per
 //         thread (TMEM lanes 32*(w%4)..+31), so no cross-warp reduction is
 //         needed, and the two groups run out of phase with each other.
-// TMEM (464 of 512 columns): S 128 | O_A 144 | O_B 144 | scale factors.
-// P^ scales are written by the softmax threads straight into TMEM
-// (tcgen05.st): an M=128 block-scaled MMA reads row r's A scales from lane r,
-// column base + r/32.
+// TMEM (496 of 512 columns): S 128 | O_A 144 | O_B 144 | scale factors 48 |
+// P^_A 16 | P^_B 16. The softmax threads write P^ straight into TMEM
+// (tcgen05.st): the codes as the A operand of P^V^ (row r in lane r, eight
+// E2M1 values per column), the scales where an M=128 block-scaled MMA reads
+// row r's A scales (lane r, column base + r/32). The NVFP4 kernels, whose
+// scale factors take the last 96 columns, keep P^ in shared memory.
 //
 // Causal mode (MatX note "leaky quantization"): keys j > i are masked before
 // the maximum, tiles past the diagonal are skipped, and for the 32-token V
@@ -60,7 +62,7 @@ constexpr uint32_t kVTileBytes = kPvN * kD / 2;  // 9216
 constexpr uint32_t kOffQ = 0;                                 // 2 tiles
 constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;            // kKStages tiles
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;     // kVStages tiles (+ ones rows)
-constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]
+constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]: NVFP4 P^; epilogue staging
 constexpr int kNumBars = 40;
 // Scale atoms, barriers and TMEM scale columns per operand format: MXFP4 has
 // one 512-byte atom per 128-row tile (4 blocks of 32 per row, both K halves in
@@ -87,6 +89,11 @@ struct Lay {
   static constexpr uint32_t kColSFK = kNv ? 432 : 424;
   static constexpr uint32_t kColSFP = kNv ? 448 : 432;
   static constexpr uint32_t kColSFV = kNv ? 480 : 448;  // per buffer (x MMA): data atom, then the ones atom at +4
+  // MXFP4: the P^ codes of group g (the A operand of its P^V^, 128 keys = 16
+  // columns of eight E2M1 values per row) at kColPT + 16 g; NVFP4 keeps P^ in
+  // shared memory (its scale factors fill TMEM)
+  static constexpr uint32_t kColPT = 464;
+  static_assert(kNv || (kColSFV + 16 <= kColPT && kColPT + 32 <= 512), "TMEM columns overlap");
 };
 
 // mbarrier indices
@@ -280,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kOffQSF = L::kOffQSF, kOffKSF = L::kOffKSF, kOffVSF = L::kOffVSF, kOffOnesSF = L::kOffOnesSF;
   constexpr uint32_t kOffBars = L::kOffBars, kOffMisc = L::kOffMisc, kSfTile = L::kSfTile;
   constexpr uint32_t kColSFQ = L::kColSFQ, kColSFK = L::kColSFK, kColSFP = L::kColSFP, kColSFV = L::kColSFV;
+  constexpr uint32_t kColPT = L::kColPT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id0 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 0, 0);
       const uint32_t id1 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 2, 2);
-      const uint64_t dp0 = smem_desc(sb + kOffP, 16, 512, kSwizzle64B);
+      [[maybe_unused]] const uint64_t dp0 = smem_desc(sb + kOffP, 16, 512, kSwizzle64B);
       const uint64_t dv0 = smem_desc(sb + kOffV, 16, 512, kSwizzle64B);
       const uint64_t dsfv0 = smem_desc(sb + kOffVSF, 0, 128, kSwizzleNone);
       // scale atom of the ones rows, once into both V scale buffers (each K half for NVFP4)
@@ -484,16 +492,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kNv) tc_cp_sf(sfv + 8, dsfv0 + vs * (kSfTile >> 4) + (kSfAtomBytes >> 4));
             sfv_loaded = true;
           }
-          const uint64_t dp = dp0 + (2 * g + (j & 1)) * (kTileBytes >> 4);
           const uint32_t od = tmem + kColO + g * kPvN;
           if constexpr (kNv) {
+            const uint64_t dp = dp0 + (2 * g + (j & 1)) * (kTileBytes >> 4);
             const uint32_t sfp = tmem + kColSFP + 16 * g + 8 * (j & 1);
             mma_nvf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
             mma_nvf4(od, dp + 2, dv + 2, id1, sfp + 4, sfv + 8, 1u);
           } else {
+            // P^ from TMEM: keys 0-63 in the group's first 8 columns, 64-127 in the next 8
+            const uint32_t pa = tmem + kColPT + 16 * g;
             const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
-            mma_mxf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
-            mma_mxf4(od, dp + 2, dv + 2, id1, sfp, sfv, 1u);
+            mma_mxf4_ta(od, pa, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
+            mma_mxf4_ta(od, pa + 8, dv + 2, id1, sfp, sfv, 1u);
           }
           tc_commit(bar(kBarODone + g));
         }
@@ -536,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < Tg && !my_abort; j++) {
       const int pb = j & 1;
       float v[128];
+      uint32_t pw[16];  // MXFP4: the row's P^ codes (eight per word), stored to TMEM after o_done
       wait_uniform(kBarSFull + g, j & 1);
       if (my_abort) break;
       tc_fence_after();
@@ -716,13 +727,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_new = fmaxf(fmax3(m_run, bm[0], bm[1]), fmaxf(bm[2], bm[3]));
         const float mc = m_new * C;
 
-        // The P^ buffer and TMEM scale columns of parity pb were last read by P^V^ of
-        // tile j-2; this thread saw that product complete in its o_done wait of tile j-1.
+        // The TMEM scale columns of parity pb were last read by P^V^ of tile j-2;
+        // this thread saw that product complete in its o_done wait of tile j-1.
+        // The codes stay in registers until P^V^ of tile j-1, the last reader of
+        // the group's one P^ buffer in TMEM, is complete.
         // P^ = Q*(exp(S/sqrt(d) - m_new)) per 32-key block with the UOS scale of the
         // block maximum. Branch-free: a fully masked block has max -inf, all its
         // exponentials are 0 and it takes the all-zero-block scale (byte 127).
-        uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
-        const int swz = (r >> 1) & 3;
         const bool diag_tile = kCausal && j == Tg - 1;
         uint8_t* dump = (kDump && qrow < N)
                             ? p.phat_codes + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 64
@@ -814,7 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             diag_sbyte = (sbytes >> (8 * b)) & 0xFFu;
           }
-          *reinterpret_cast<uint4*>(prow + ((b ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int gq = 0; gq < 4; gq++) pw[4 * b + gq] = w[gq];
         }
         };
         if (kCausal && diag_tile)
@@ -824,9 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kDump && dump != nullptr)
           *reinterpret_cast<uint32_t*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 4) = sbytes;
         // P^ scales: lane r, column base + r/32 of this group's scale buffer
-        // (the store is waited for with the O rescale's, before p_full)
+        // (the store is waited for with the codes' and O rescale's, before p_full)
         tmem_st1(tl + kColSFP + 8 * g + 4 * pb + quad, sbytes);
-        fence_proxy_async_smem();
       }
       if constexpr (kVariant) l_direct = fmaf(ex2_approx((m_run - m_new) * C), l_direct, tile_ptilde);
       if (j >= 1) {
@@ -835,6 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_uniform(kBarODone + g, (j - 1) & 1);
         if (my_abort) break;
         tc_fence_after();
+        if constexpr (!kNv) tmem_st16(tl + kColPT + 16 * g, pw);
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
           // O_g row (128 columns + l) *= alpha: all loads in flight at once, one wait
           const float2 a2 = make_float2(alpha, alpha);
@@ -872,6 +884,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tl + ocol + 96, o3);
           tmem_st1(tl + ocol + kD, __float_as_uint(__uint_as_float(l) * alpha));
         }
+      } else if constexpr (!kNv) {
+        tmem_st16(tl + kColPT + 16 * g, pw);
       }
       tmem_wait_st();
       tc_fence_before();
