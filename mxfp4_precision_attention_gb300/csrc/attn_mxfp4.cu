@@ -24,8 +24,9 @@
 // P^_A 16 | P^_B 16. The softmax threads write P^ straight into TMEM
 // (tcgen05.st): the codes as the A operand of P^V^ (row r in lane r, eight
 // E2M1 values per column), the scales where an M=128 block-scaled MMA reads
-// row r's A scales (lane r, column base + r/32). The NVFP4 kernels, whose
-// scale factors take the last 96 columns, keep P^ in shared memory.
+// row r's A scales (lane r, column base + r/32). The NVFP4 kernels (two scale
+// words per operand row, one per K half) keep one buffer of P^ and V^ scales
+// to make room for the two P^ operands.
 //
 // Causal mode (MatX note "leaky quantization"): keys j > i are masked before
 // the maximum, tiles past the diagonal are skipped, and for the 32-token V
@@ -62,7 +63,7 @@ constexpr uint32_t kVTileBytes = kPvN * kD / 2;  // 9216
 constexpr uint32_t kOffQ = 0;                                 // 2 tiles
 constexpr uint32_t kOffK = kOffQ + 2 * kTileBytes;            // kKStages tiles
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;     // kVStages tiles (+ ones rows)
-constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]: NVFP4 P^; epilogue staging
+constexpr uint32_t kOffP = kOffV + kVStages * kVTileBytes;    // [2 groups][2 buffers]: epilogue staging
 constexpr int kNumBars = 40;
 // Scale atoms, barriers and TMEM scale columns per operand format: MXFP4 has
 // one 512-byte atom per 128-row tile (4 blocks of 32 per row, both K halves in
@@ -84,16 +85,16 @@ struct Lay {
   static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   // TMEM scale columns (S at 0, O_A and O_B at 128 .. 415)
   //   MXFP4: Q [2 groups] x 4 | K [2 buffers] x 4 | P [2 groups][2 buffers] x 4 | V [2 buffers] x 8
-  //   NVFP4: each of those x 2 MMAs (K halves): 416 | 432 | 448 | 480, up to 512
+  //   NVFP4, two MMAs (K halves) each: Q [2 groups] x 8 | K [2 buffers] x 8 | P [2 groups] x 8 | V x 16
+  //   (its P^ and V^ scales have one buffer: 416 | 432 | 448 | 464)
   static constexpr uint32_t kColSFQ = 416;
   static constexpr uint32_t kColSFK = kNv ? 432 : 424;
   static constexpr uint32_t kColSFP = kNv ? 448 : 432;
-  static constexpr uint32_t kColSFV = kNv ? 480 : 448;  // per buffer (x MMA): data atom, then the ones atom at +4
-  // MXFP4: the P^ codes of group g (the A operand of its P^V^, 128 keys = 16
-  // columns of eight E2M1 values per row) at kColPT + 16 g; NVFP4 keeps P^ in
-  // shared memory (its scale factors fill TMEM)
-  static constexpr uint32_t kColPT = 464;
-  static_assert(kNv || (kColSFV + 16 <= kColPT && kColPT + 32 <= 512), "TMEM columns overlap");
+  static constexpr uint32_t kColSFV = kNv ? 464 : 448;  // per buffer (x MMA): data atom, then the ones atom at +4
+  // the P^ codes of group g (the A operand of its P^V^, 128 keys = 16 columns
+  // of eight E2M1 values per row) at kColPT + 16 g
+  static constexpr uint32_t kColPT = kNv ? 480 : 464;
+  static_assert(kColSFV + 16 <= kColPT && kColPT + 32 <= 512, "TMEM columns overlap");
 };
 
 // mbarrier indices
@@ -464,12 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id0 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 0, 0);
       const uint32_t id1 = kNv ? idesc_nvf4(128, kPvN) : idesc_mxf4(128, kPvN, 2, 2);
-      [[maybe_unused]] const uint64_t dp0 = smem_desc(sb + kOffP, 16, 512, kSwizzle64B);
       const uint64_t dv0 = smem_desc(sb + kOffV, 16, 512, kSwizzle64B);
       const uint64_t dsfv0 = smem_desc(sb + kOffVSF, 0, 128, kSwizzleNone);
-      // scale atom of the ones rows, once into both V scale buffers (each K half for NVFP4)
+      // scale atom of the ones rows, once into the V scale buffers (each K half for NVFP4)
       if constexpr (kNv) {
-        for (int i = 0; i < 4; i++) tc_cp_sf(tmem + kColSFV + 8 * i + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
+        for (int i = 0; i < 2; i++) tc_cp_sf(tmem + kColSFV + 8 * i + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
       } else {
         tc_cp_sf(tmem + kColSFV + 4, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
         tc_cp_sf(tmem + kColSFV + 12, smem_desc(sb + kOffOnesSF, 0, 128, kSwizzleNone));
@@ -479,28 +479,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vs = j % kVStages;
         if (!mbar_wait(bar(kBarVFull + vs), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
         const uint64_t dv = dv0 + vs * (kVTileBytes >> 4);
-        const uint32_t sfv = tmem + kColSFV + (kNv ? 16 : 8) * (j & 1);
+        const uint32_t sfv = tmem + kColSFV + (kNv ? 0 : 8 * (j & 1));
         bool sfv_loaded = false;
         for (int g = 0; g < 2; g++) {
           if (j >= (g ? ntiles1 : ntiles0)) continue;
           if (!mbar_wait(bar(kBarPFull + g), j & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           if (!sfv_loaded) {
-            // the previous user of this buffer (tile j-2) is complete: the softmax
-            // threads waited for it before arriving on p_full
+            // MXFP4: the previous user of this buffer (tile j-2) is complete: the
+            // softmax threads waited for it before arriving on p_full. NVFP4 has
+            // one buffer, last read by tile j-1's products: its V ring stage's
+            // release (committed after them) says they are complete. That
+            // barrier's previous phase (tile j-5) completed before the producer
+            // refilled the stage for tile j-1, so the parity is unambiguous.
+            if (kNv && j >= 1) {
+              if (!mbar_wait(bar(kBarVEmpty + (j - 1) % kVStages), ((j - 1) / kVStages) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
             tc_cp_sf(sfv, dsfv0 + vs * (kSfTile >> 4));
             if constexpr (kNv) tc_cp_sf(sfv + 8, dsfv0 + vs * (kSfTile >> 4) + (kSfAtomBytes >> 4));
             sfv_loaded = true;
           }
           const uint32_t od = tmem + kColO + g * kPvN;
+          // P^ from TMEM: keys 0-63 in the group's first 8 columns, 64-127 in the next 8
+          const uint32_t pa = tmem + kColPT + 16 * g;
           if constexpr (kNv) {
-            const uint64_t dp = dp0 + (2 * g + (j & 1)) * (kTileBytes >> 4);
-            const uint32_t sfp = tmem + kColSFP + 16 * g + 8 * (j & 1);
-            mma_nvf4(od, dp, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
-            mma_nvf4(od, dp + 2, dv + 2, id1, sfp + 4, sfv + 8, 1u);
+            const uint32_t sfp = tmem + kColSFP + 8 * g;
+            mma_nvf4_ta(od, pa, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
+            mma_nvf4_ta(od, pa + 8, dv + 2, id1, sfp + 4, sfv + 8, 1u);
           } else {
-            // P^ from TMEM: keys 0-63 in the group's first 8 columns, 64-127 in the next 8
-            const uint32_t pa = tmem + kColPT + 16 * g;
             const uint32_t sfp = tmem + kColSFP + 8 * g + 4 * (j & 1);
             mma_mxf4_ta(od, pa, dv, id0, sfp, sfv, j > 0 ? 1u : 0u);
             mma_mxf4_ta(od, pa + 8, dv + 2, id1, sfp, sfv, 1u);
@@ -546,7 +556,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < Tg && !my_abort; j++) {
       const int pb = j & 1;
       float v[128];
-      uint32_t pw[16];  // MXFP4: the row's P^ codes (eight per word), stored to TMEM after o_done
+      uint32_t pw[16];  // the row's P^ codes (eight per word), stored to TMEM after o_done
+      uint32_t sfw[2] = {0u, 0u};  // NVFP4: the row's P^ scale words (K halves), stored with the codes
+      // the P^ operand of this tile's P^V^ into the group's one TMEM buffer (its
+      // last reader, P^V^ of tile j-1, is complete); NVFP4's scale words go with
+      // it (one buffer too; MXFP4's are double-buffered and stored earlier).
+      // Scales: lane r, column base + r/32 of each K half's word
+      auto store_phat = [&]() {
+        tmem_st16(tl + kColPT + 16 * g, pw);
+        if constexpr (kNv) {
+          tmem_st1(tl + kColSFP + 8 * g + quad, sfw[0]);
+          tmem_st1(tl + kColSFP + 8 * g + 4 + quad, sfw[1]);
+        }
+      };
       wait_uniform(kBarSFull + g, j & 1);
       if (my_abort) break;
       tc_fence_after();
@@ -646,8 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 8; b++) bm[b] = bm_ld[b];
         m_new = fmax3(fmax3(m_run, bm[0], bm[1]), fmax3(bm[2], bm[3], bm[4]), fmax3(bm[5], bm[6], bm[7]));
         const float mc = m_new * C;
-        uint8_t* prow = smem + kOffP + (2 * g + pb) * kTileBytes + r * 64;
-        const int swz = (r >> 1) & 3;
         const bool diag_tile = kCausal && j == Tg - 1;
         const float2 c2 = make_float2(C, C);
         uint8_t* dump = (kDump && qrow < N)
@@ -710,16 +730,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             w[3] = hi ? 0u : w[3];
             diag_s = hi ? sv[2 * c + 1] : sv[2 * c];
           }
-          *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int k = 0; k < 4; k++) pw[4 * c + k] = w[k];
         }
         if (kDump && dump != nullptr)
           *reinterpret_cast<uint2*>(p.phat_scales + ((static_cast<int64_t>(bh) * N + qrow) * p.NT + j) * 8) =
               make_uint2(sw[0], sw[1]);
-        // P^ scales: lane r, column base + r/32 of each K half's scale word
-        tmem_st1(tl + kColSFP + 16 * g + 8 * pb + quad, sw[0]);
-        tmem_st1(tl + kColSFP + 16 * g + 8 * pb + 4 + quad, sw[1]);
-        fence_proxy_async_smem();
-        tmem_wait_st();
+        sfw[0] = sw[0];
+        sfw[1] = sw[1];
       } else {
         float bm[4];
 #pragma unroll
@@ -846,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_uniform(kBarODone + g, (j - 1) & 1);
         if (my_abort) break;
         tc_fence_after();
-        if constexpr (!kNv) tmem_st16(tl + kColPT + 16 * g, pw);
+        store_phat();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
           // O_g row (128 columns + l) *= alpha: all loads in flight at once, one wait
           const float2 a2 = make_float2(alpha, alpha);
@@ -884,8 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tl + ocol + 96, o3);
           tmem_st1(tl + ocol + kD, __float_as_uint(__uint_as_float(l) * alpha));
         }
-      } else if constexpr (!kNv) {
-        tmem_st16(tl + kColPT + 16 * g, pw);
+      } else {
+        store_phat();
       }
       tmem_wait_st();
       tc_fence_before();

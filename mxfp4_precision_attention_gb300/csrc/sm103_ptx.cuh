@@ -220,7 +220,18 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
 }
-// The same with the A operand (M rows x 64 E2M1 values, 8 per 32-bit column,
+// NVFP4 (kind::mxf4nvf4, scale_vec::4X) with the A operand read from tensor
+// memory (M rows x 64 E2M1 values, 8 per 32-bit column, lane = row).
+__device__ __forceinline__ void mma_nvf4_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// MXFP4 with the A operand (M rows x 64 E2M1 values, 8 per 32-bit column,
 // lane = row) read from tensor memory.
 __device__ __forceinline__ void mma_mxf4_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
