@@ -942,7 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv_lo = kNv ? inv_l * vdq : inv_l;  // O from the tensor cores carries V's encode factor
         // O / l of the warp's 32 rows to global memory in whole 128-byte lines:
         // each 32-column chunk goes through the warp's own rows of the group's
-        // two P^ buffers (free: every P^V^ of the group has completed), rows
+        // two 8 KB staging buffers in shared memory (the region that held P^
+        // when it went through shared memory; unused by the key loop), rows
         // 0-15 in the first and 16-31 in the second, 16-byte units swizzled by
         // row % 8 (the 128-byte swizzle of a TMA box). The non-causal kernels
         // then store each half with one TMA copy (rows past N are clipped) and
@@ -1128,9 +1129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 32-channel chunk (2 KB) at a time: lane t loads key t's 64 bytes of
           // the chunk, the next chunk's loads are in flight while this one is
           // used, and every thread then reads all 32 rows as broadcasts. The
-          // staging space is this group's two P^ buffers, idle since the o_done
-          // wait above (every P^V^ that read them has completed): 4 KB per warp,
-          // two chunk slots.
+          // staging space is this group's two 8 KB staging buffers (unused by
+          // the key loop): 4 KB per warp, two chunk slots.
           float* orow = p.out + (static_cast<int64_t>(bh) * N + qrow) * kD;
           uint8_t* stage = smem + kOffP + 2 * g * kTileBytes + quad * 4096;
           const int64_t mykey = static_cast<int64_t>(Tg - 1) * kTile + 32 * quad + lane;
