@@ -208,6 +208,15 @@ def test_nvfp4_forward_full_size_sampled(mx, orc, name, nrows):
     assert err <= TOL_REL_RMS * rms
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_nvfp4_forward_all_rows_past_two_ring_wraps(mx, orc, causal):
+    """Nine key tiles (N = 1100): the 4-stage V ring wraps twice. The NVFP4 kernel keeps
+    one buffer of V^ scales in TMEM and reloads it once the previous tile's products are
+    complete, which it learns from that tile's ring release; every row against the oracle."""
+    q, k, v = W.generate(W.WORKLOADS["causal_lm_8192"], device="cuda", B=1, H=1, N=1100, seed=23)
+    _nv_parity(mx, orc, q, k, v, causal, 1, f"nvfp4 N=1100 causal={causal}")
+
+
 @pytest.mark.parametrize("N", [1, 17, 128, 129, 257])
 @pytest.mark.parametrize("causal", [False, True])
 def test_nvfp4_forward_tiny_and_ragged_lengths(mx, orc, N, causal):
