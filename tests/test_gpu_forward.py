@@ -201,6 +201,36 @@ def test_v_ones_gives_ones(mx):
         assert torch.max(torch.abs(out - 1.0)).item() <= 1e-6
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_scores_give_block_means(mx, orc, causal):
+    """Degenerate case (Q = 0: every score 0, P~ = 1, P^ = 1 exactly, l = visible
+    keys): O is the mean of the visible V^ rows, with the query's own 32-token
+    block on its bf16 V rows in causal mode. The reference is that closed form
+    over the oracle's V^, not a replay of the kernel; N is ragged."""
+    B, H, N = 1, 2, 1000
+    _, k, v = W.generate(W.WORKLOADS["lognormal_4096"], device="cuda", B=B, H=H, N=N, seed=41)
+    q = torch.zeros_like(k)
+    out = _gpu_mx(mx, q, k, v, causal=causal).reshape(B * H, N, 128).cpu().numpy().astype(np.float64)
+    v16 = W.as_u16(v.reshape(B * H, N, 128))
+    vc, vs = orc.quantize_v(v16)
+    e2 = np.array([orc.e2m1_value(c) for c in range(16)])
+    blk = np.arange(N) // 32
+    vhat = e2[vc] * np.transpose(np.exp2(vs.astype(np.float64) - 127.0)[:, :, blk], (0, 2, 1))
+    vraw = v.reshape(B * H, N, 128).float().cpu().numpy().astype(np.float64)
+    if causal:
+        csum = np.cumsum(vhat, axis=1)
+        want = np.empty_like(vhat)
+        for i in range(N):
+            d0 = 32 * (i // 32)
+            off = csum[:, d0 - 1] if d0 > 0 else 0.0
+            want[:, i] = (off + vraw[:, d0:i + 1].sum(axis=1)) / (i + 1)
+    else:
+        want = np.broadcast_to(vhat.mean(axis=1, keepdims=True), vhat.shape)
+    err = np.abs(out - want).max()
+    print(f"uniform scores causal={causal}: max|O - mean| {err:.3e} (max|V| {np.abs(vraw).max():.3f})")
+    assert err <= 1e-5 * np.abs(vraw).max()
+
+
 def test_ell_consistency_direct_vs_dump(mx, orc):
     """l_i >= 1 (Appendix J) through the kernel: rows whose max entry sits in
     any tile keep an exact 1 in P^; the dumped P^ shows it."""

@@ -285,3 +285,42 @@ def test_sdpa_closed_forms(orc):
     # row 0 of a causal pass sees only key 0
     out0 = orc.sdpa(_bf16(qq), _bf16(kk), _bf16(vv), np.array([[0, 0]]), causal=True)
     assert np.allclose(out0[0], 3.0, rtol=0, atol=0)
+
+
+def _vhat(orc, vc, vs):
+    """Dequantized V^ [BH, N, 128] from the oracle's codes [BH, N, 128] and E8M0 scales [BH, 128, nblk]."""
+    e2 = np.array([orc.e2m1_value(c) for c in range(16)])
+    N = vc.shape[1]
+    sc = np.exp2(vs.astype(np.float64) - 127.0)  # [BH, 128, nblk]
+    blk = np.arange(N) // 32
+    return e2[vc] * np.transpose(sc[:, :, blk], (0, 2, 1))
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+def test_uniform_scores_give_block_means(orc, causal):
+    """Degenerate case: Q = 0 makes every score 0, so m = 0 and P~ = 1 in every
+    block; the UOS scale of a block whose maximum is 1 is 2^-2 and 1 / 2^-2 = 4
+    is an E2M1 grid point, so P^ = 1 exactly (Eq. 44) and l counts the visible
+    keys (Eq. 47). O is then the plain mean of the visible V^ rows (Eq. 48);
+    in causal mode the query's own 32-token block contributes its bf16 V rows
+    instead (the diagonal-block reading)."""
+    rng = np.random.default_rng(31)
+    N = 300
+    q = np.zeros((1, N, D))
+    k = rng.standard_normal((1, N, D)) * 3
+    v = rng.standard_normal((1, N, D))
+    q16, k16, v16 = _bits(q), _bits(k), _bits(v)
+    rows = np.array([[0, i] for i in range(N)])
+    out = _pipeline(orc, q16, k16, v16, rows, causal=causal)
+    vc, vs = orc.quantize_v(v16)
+    vhat = _vhat(orc, vc, vs)[0]
+    vraw = _bf16_vals(v16)[0]
+    for i in range(N):
+        if not causal:
+            want, ell = vhat.mean(axis=0), N
+        else:
+            d0 = 32 * (i // 32)
+            want = (vhat[:d0].sum(axis=0) + vraw[d0:i + 1].sum(axis=0)) / (i + 1)
+            ell = i + 1
+        assert np.allclose(out["out"][i], want, rtol=0, atol=1e-12 * np.abs(vraw).max())
+        assert out["ell"][i] == ell
