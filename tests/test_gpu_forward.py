@@ -108,17 +108,21 @@ def test_forward_all_rows_and_phat(mx, orc, case):
     _gate(g, ref["out"], case)
 
 
+@pytest.mark.parametrize("direction", ["rising", "falling"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_forward_rising_maxima_rescale_every_tile(mx, orc, causal):
+def test_forward_rising_maxima_rescale_every_tile(mx, orc, causal, direction):
     """Scores that grow along the keys (K_j = s_j * u + noise, Q_i = u + noise, s_j
     increasing): every key tile raises every row's running maximum, so each
     softmax warp rescales O and l in TMEM on every tile (Eqs. 3-5) and every
-    P^ is taken relative to a new m. All rows and every P^ entry against the
-    oracle; N = 900 (eight tiles, the last ragged)."""
+    P^ is taken relative to a new m. Falling scores are the opposite case: the
+    maximum is set in the first tile and no later tile rescales. All rows and
+    every P^ entry against the oracle; N = 900 (eight tiles, the last ragged)."""
     B, H, N = 1, 2, 900
     g = torch.Generator().manual_seed(53)
     u = torch.randn(B, H, 1, 128, generator=g)
     s = torch.linspace(0.0, 1.0, N).reshape(1, 1, N, 1)
+    if direction == "falling":
+        s = 1.0 - s
     q = (u + 0.1 * torch.randn(B, H, N, 128, generator=g)).to(torch.bfloat16).cuda()
     k = (s * u + 0.1 * torch.randn(B, H, N, 128, generator=g)).to(torch.bfloat16).cuda()
     v = torch.randn(B, H, N, 128, generator=g).to(torch.bfloat16).cuda()
@@ -127,9 +131,9 @@ def test_forward_rising_maxima_rescale_every_tile(mx, orc, causal):
     ref = _oracle(orc, q, k, v, rows, causal=causal, want_phat=True)
     got = out.reshape(B * H, N, 128).cpu().numpy().astype(np.float64)[rows[:, 0], rows[:, 1]]
     rate, nflip = _flip_rate(orc, pc, ps, ref["phat"], rows, N, causal)
-    print(f"rising maxima causal={causal}: P^ flip rate {rate:.2e} ({nflip} entries)")
+    print(f"{direction} maxima causal={causal}: P^ flip rate {rate:.2e} ({nflip} entries)")
     assert rate < MAX_FLIP_RATE
-    _gate(got, ref["out"], f"rising maxima causal={causal}")
+    _gate(got, ref["out"], f"{direction} maxima causal={causal}")
 
 
 def test_forward_lognormal_sampled(mx, orc):
